@@ -1,0 +1,437 @@
+"""Benchmark: selective-SSM prefill tokens/s on one GB300 (plus decode steps/s and the q8 reduction).
+
+One step = one ssm_prefill over the Mamba-130M-like layer workload (batch 4, 2048
+tokens, d_inner 1536, d_state 16, conv 4; bf16 x/z/dt/B/C, fp32 A/D/states, fp32
+out), inputs resident in HBM, L2 flushed (a 2x-L2 buffer write) before every timed
+step, each step timed with CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the
+workload (the mixer shards by channel and by batch row with no exchange), the
+ranks meet only at the timing barriers, and value = all ranks' tokens / the
+slowest rank's time ("weak" scaling).  ``--impl reference`` times the fp64 CPU
+oracle on this host's cores on the same workload instead.
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+WORKLOAD = dict(name="mamba130m_like_prefill", batch=4, seqlen=2048, d_inner=1536, d_state=16, d_conv=4)
+METRIC = "prefill tokens/s and decode steps/s per layer; achieved HBM GB/s vs 8 TB/s"
+UNIT = "tokens/s"
+
+
+# ---------------------------------------------------------------- algorithmic cost model
+def prefill_bytes(batch, L, D, in_es=2, out_es=4):
+    """Bytes the prefill must move: x, z, dt in + out per (t, d); B, C per token; params per
+    channel (A 64 + D, dt_bias, conv_b 12 + conv_w 16 = 92 B); final states per (b, d) (64 + 12 B)."""
+    return (batch * L * D * (3 * in_es + out_es) + batch * L * 2 * 16 * in_es + D * 92 + batch * D * 76)
+
+
+def prefill_fp32_ops(batch, L, D):
+    """FP32-pipe operations the plain sequential recurrence needs: per (t, d, n) delta*A, (delta u)*B,
+    the state FMA and the C readout FMA (4 x 16 = 64); per (t, d) ~20 for conv, SiLU, softplus, skip
+    and gate arithmetic."""
+    return batch * L * D * (4 * 16 + 20)
+
+
+def decode_bytes(batch, D, in_es=2, out_es=4):
+    """ssm state 64 B read + 64 B write, conv state 12 + 12 B, x/z/dt, out per (r, d); params per
+    channel; B, C per request."""
+    return batch * D * (128 + 24 + 3 * in_es + out_es) + D * 92 + batch * 2 * 16 * in_es
+
+
+def q8_bytes(P, n, in_es=2, out_es=2):
+    return P * n * in_es + n * out_es + n * 4 + ((n + 127) // 128) * 4
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _cpu_oracle_run(inp, budget_s, threads):
+    """Run the fp64 oracle over the whole workload until `budget_s` has elapsed (at least once)."""
+    import oracle
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w,
+                       inp.conv_b, n_threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return reps, el
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args):
+    import torch
+    rank, _, world = _dist()
+    if rank != 0:
+        return
+    from selective_state_space_prefill_gb300.inputs import make_mixer_inputs
+    import oracle
+    w = WORKLOAD
+    inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=torch.bfloat16, seed=0)
+    threads = _host_cores()
+    oracle.build()
+    for _ in range(args.warmup):
+        _cpu_oracle_run(inp, 0.0, threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _cpu_oracle_run(inp, 0.0, threads)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    tokens = w["batch"] * w["seqlen"] * args.steps
+    value = tokens / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) tokens, Mamba-style parameters)",
+        "config": {"workload": w["name"], "batch": w["batch"], "seq_len": w["seqlen"], "d_inner": w["d_inner"],
+                   "d_state": 16, "d_conv": 4, "inputs": "bf16"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "the whole workload (all 1536 channels x 4 x 2048 tokens) per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local, world = _dist()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libssm has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from selective_state_space_prefill_gb300 import build as ssm_build
+    if not ssm_build.up_to_date():
+        if world > 1:
+            raise SystemExit("libssm.so is not built: run __graft_entry__.build() before torchrun")
+        ssm_build.build()
+    from selective_state_space_prefill_gb300 import binding as ssm
+    from selective_state_space_prefill_gb300.inputs import make_mixer_inputs, make_partials, make_states, \
+        make_decode_inputs, make_mixer_params
+
+    w = WORKLOAD
+    B, L, D = w["batch"], w["seqlen"], w["d_inner"]
+    inp = make_mixer_inputs(B, L, D, dtype=torch.bfloat16, seed=0, device=dev)
+    out = torch.empty(B, L, D, device=dev, dtype=torch.float32)
+    cso = torch.empty(B, 3, D, device=dev)
+    sso = torch.empty(B, D, 16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w, inp.conv_b,
+                    out=out, conv_state_out=cso, ssm_state_out=sso, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(float(k))          # evict the inputs from L2 between timed steps
+            evs[k][0].record(stream)
+            step()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+        time.sleep(0.25)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    dev_s = sum(step_ms) / 1e3
+    if world > 1:
+        dist.barrier()
+        t = torch.tensor([dev_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_s = float(t.item())
+    tokens = world * B * L * args.steps
+    value = tokens / dev_s
+    ms_per_step = 1e3 * dev_s / args.steps
+    status = ssm.device_status(clear=True)
+
+    # ---- roofline of the prefill kernel (the only kernel of the step)
+    hbm_peak, peak_kind = _peaks()
+    abytes = prefill_bytes(B, L, D)
+    avg_s = statistics.mean(step_ms) / 1e3
+    achieved_gbs = abytes / avg_s / 1e9
+    props = torch.cuda.get_device_properties(dev)
+    n_sm = props.multi_processor_count
+    cs = clocks.summary()
+    sm_max = cs["sm_max_mhz"] or 2070.0
+    fp32_peak = n_sm * 128 * sm_max * 1e6 / 1e12           # TFLOP/s-equivalent: FP32-pipe lane-ops/s
+    fp32_ach = prefill_fp32_ops(B, L, D) / avg_s / 1e12
+    roofline = {"bound": "alu", "achieved": fp32_ach, "peak": fp32_peak, "unit": "T fp32-ops/s",
+                "frac": fp32_ach / fp32_peak, "traffic": None,
+                "kernel": "k_prefill", "peak_source": f"{n_sm} SMs x 128 FP32 lanes x {sm_max:.0f} MHz",
+                "hbm": {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": achieved_gbs / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                        "algorithmic_bytes_per_launch": abytes}}
+
+    # ---- end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(inp, k).cpu().pin_memory() for k in ("x", "z", "dt", "B", "C")}
+        dbuf = {k: torch.empty_like(getattr(inp, k)) for k in host}
+        hout = torch.empty(B, L, D, dtype=torch.float32).pin_memory()
+        hcs = torch.empty(B, 3, D).pin_memory()
+        hss = torch.empty(B, D, 16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = hout.numel() * 4 + hcs.numel() * 4 + hss.numel() * 4
+
+        def e2e_step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            ssm.prefill(dbuf["x"], dbuf["z"], dbuf["dt"], dbuf["B"], dbuf["C"], inp.A, inp.D, inp.dt_bias,
+                        inp.conv_w, inp.conv_b, out=out, conv_state_out=cso, ssm_state_out=sso, stream=stream)
+            hout.copy_(out, non_blocking=True)
+            hcs.copy_(cso, non_blocking=True)
+            hss.copy_(sso, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        es = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([es], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            es = float(t.item())
+        e2e = {"value": world * B * L * args.steps / es, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    # ---- decode steps/s (batch 1/8/64/256 x d_inner 8192, CUDA graph of 64 steps) and the q8 reduction
+    extras = {}
+    if not args.no_extras:
+        extras["decode"] = bench_decode(ssm, dev, stream, hbm_peak)
+        extras["q8"] = bench_q8(ssm, dev, stream, hbm_peak, flush)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        cpu_inp = inp.to("cpu")
+        threads = _host_cores()
+        reps, el = _cpu_oracle_run(cpu_inp, args.cpu_seconds, threads)
+        cpu = {"value": reps * B * L / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"the whole workload (all {D} channels x {B} x {L} tokens), {reps} run(s) in {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) tokens; A=-(n+1), D=1, log-uniform dt_bias, U(-.5,.5) conv)",
+            "config": {"workload": w["name"], "batch": B, "seq_len": L, "d_inner": D, "d_state": 16, "d_conv": 4,
+                       "inputs": "bf16 x/z/dt/B/C, fp32 params and states", "out": "fp32",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed before every timed step (write of a 2x-L2 buffer)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": {k: cs[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "wall_s_timed_region": t_wall, "device_status": status,
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_decode(ssm, dev, stream, hbm_peak, steps=64, D=8192):
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_decode_inputs, make_mixer_params, make_states
+    res = {}
+    par = {k: v.to(dev) for k, v in make_mixer_params(D, seed=1).items()}
+    for batch in (1, 8, 64, 256):
+        tok = {k: v.to(dev) for k, v in make_decode_inputs(batch, D, seed=batch).items()}
+        cs, ss = (t.to(dev) for t in make_states(batch, D, seed=batch))
+        out = torch.empty(batch, D, device=dev)
+
+        def one():
+            ssm.decode_step(tok["x"], tok["z"], tok["dt"], tok["B"], tok["C"], par["A"], par["D"], par["dt_bias"],
+                            par["conv_w"], par["conv_b"], cs, ss, out=out, stream=torch.cuda.current_stream(dev))
+
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                one()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(steps):
+                one()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) / 1e3 / (reps * steps)
+        gbs = decode_bytes(batch, D) / t / 1e9
+        res[f"batch{batch}"] = {"steps_per_s": 1.0 / t, "us_per_step": 1e6 * t, "GB_s": gbs,
+                                "frac_hbm": gbs / hbm_peak}
+    res["note"] = ("d_inner 8192, bf16 tokens, fp32 states in place; CUDA graph of 64 back-to-back steps; "
+                   "states of batch <= 64 stay L2-resident between steps")
+    return res
+
+
+def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4):
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_partials
+    res = {}
+    for batch in (1, 8, 64, 256, 4096):
+        n = batch * 4096
+        parts = [p.to(dev) for p in make_partials(P, (batch, 1, 4096), dtype=torch.bfloat16, seed=batch)]
+        out = torch.empty(batch, 1, 4096, device=dev, dtype=torch.bfloat16)
+        sums = torch.empty(n, device=dev, dtype=torch.int32)
+        scales = torch.empty((n + 127) // 128, device=dev)
+        for _ in range(3):
+            ssm.q8_reduce(parts, out=out, sums=sums, scales=scales, stream=stream)
+        times = []
+        for k in range(10):
+            flush.fill_(float(k))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ssm.q8_reduce(parts, out=out, sums=sums, scales=scales, stream=stream)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        t = statistics.median(a.elapsed_time(b) for a, b in times) / 1e3
+        gbs = q8_bytes(P, n) / t / 1e9
+        res[f"batch{batch}"] = {"us": 1e6 * t, "GB_s": gbs, "frac_hbm": gbs / hbm_peak}
+    res["note"] = ("P=4 bf16 partials [batch,1,4096], block 128, bf16 out + int32 sums + scales; "
+                   "L2 flushed before each call; batch 4096 is an extended size showing the bandwidth regime")
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/*
+ * ssm.h -- C ABI of libssm: the selective state-space (SSM) mixer hot path on
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What is computed.  The pages this library follows ("Scaling State-Space Models
+ * on Multiple GPUs with Tensor Parallelism", euno.news summary of arXiv
+ * 2602.21144) describe a tensor-parallel SSM layer in which
+ *   - every channel slice keeps its own hidden state, so the per-token recurrent
+ *     update needs nothing from other channels (Methodology 2, "local recurrence");
+ *   - the hidden state is cached at prefill and reused by token-by-token decode
+ *     (Methodology 3, "state caching during prefill and decode");
+ *   - partial outputs are quantized to 8 bits, summed and dequantized
+ *     (Methodology 4, "quantized All-Reduce").
+ * The pages do not print the mixer's equations; this library computes the
+ * Mamba-style selective-scan mixer.  For batch row b, channel d, token t and
+ * state n (N = d_state = 16, W = d_conv = 4):
+ *
+ *   xc_t    = conv_b[d] + sum_{k<W} conv_w[d][k] * x_{t-W+1+k}      (x_{<0}: conv_state_in or 0)
+ *   u_t     = xc_t * sigmoid(xc_t)                                   (SiLU)
+ *   delta_t = softplus(dt_t + dt_bias[d])
+ *   h_t[n]  = exp(delta_t * A[d][n]) * h_{t-1}[n] + delta_t * B_t[n] * u_t
+ *   y_t     = sum_n C_t[n] * h_t[n] + D[d] * u_t
+ *   out_t   = y_t * z_t * sigmoid(z_t)
+ *
+ * Readings where the description leaves a step open: the "x" of the input and
+ * skip terms is the post-conv, post-SiLU u; conv_w[d][W-1] multiplies the current
+ * token; the conv state holds the last W-1 raw (pre-conv) inputs, oldest first;
+ * B and C are per-token inputs shared by all channels; states start at zero when
+ * no input state is given.
+ *
+ * Conventions for every call.
+ *   - All pointers except `partials` (a host array) are DEVICE pointers owned by
+ *     the caller.  The library allocates nothing and keeps no per-call state.
+ *   - Calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Argument errors are found on the host before any launch
+ *     and return a negative status synchronously; nothing is launched then.
+ *   - Element strides are in ELEMENTS, channel stride is always 1.
+ *   - Inputs and outputs must not alias, except the in-place decode states.
+ *   - Supported: d_state == 16, d_conv == 4, d_inner % 8 == 0; token tensors
+ *     16-byte aligned with 16-byte-multiple row strides.  Other shapes return
+ *     SSM_ERR_UNSUPPORTED / SSM_ERR_MISALIGNED.
+ *   - ssm_last_error() describes the last non-OK return on the calling thread.
+ */
+#ifndef SSM_H_
+#define SSM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = -1,   /* bad size, null required pointer, bad stride */
+    SSM_ERR_UNSUPPORTED = -2,   /* valid but not implemented (d_state != 16, ...) */
+    SSM_ERR_MISALIGNED = -3,    /* pointer or stride breaks the 16-byte rule */
+    SSM_ERR_CUDA = -4,          /* a CUDA runtime/driver call or launch failed */
+    SSM_ERR_DEVICE_TIMEOUT = -5 /* reported by ssm_device_status(): an in-kernel wait gave up */
+};
+
+/* Bits of the device status word (see ssm_device_status). */
+enum {
+    SSM_DEV_WAIT_TIMEOUT = 1u,  /* a bounded wait on a TMA copy expired; the block stopped early */
+    SSM_DEV_BAD_SLOT = 2u,      /* a decode request named a state slot outside [0, n_slots) */
+    SSM_DEV_SMEM_ALIGN = 4u     /* shared memory was not 128-byte aligned; the prefill did nothing */
+};
+
+/* ABI version of this header (major * 100 + minor). */
+int ssm_abi_version(void);
+
+/*
+ * ssm_prefill -- run the mixer over `seqlen` tokens of every batch row and
+ * return the outputs plus the final conv and SSM states (the cached state of
+ * Methodology 3).  Channels are independent (Methodology 2): the result for a
+ * channel does not depend on d_inner, on which other channels are in the call,
+ * or on the launch shape, bit for bit.
+ *
+ *   batch, seqlen, d_inner       B >= 1, L >= 1, D >= 8 with D % 8 == 0
+ *   d_state, d_conv              must be 16 and 4
+ *   in_dtype                     SSM_BF16 or SSM_F32, for x, z, dt, Bmat, Cmat
+ *   out_dtype                    SSM_F32 or SSM_BF16 (round to nearest even)
+ *   x, z, dt                     [B][L][D] views: element (b, t, d) at
+ *                                b*in_stride_b + t*in_stride_t + d; in_stride_t >= D
+ *                                (a channel slice of a wider tensor is allowed);
+ *                                base 16-byte aligned, strides*size multiples of 16
+ *   Bmat, Cmat                   [B][L][16] contiguous, 16-byte aligned
+ *   A, Dskip, dt_bias            [D][16], [D], [D] float32 (A row-major, rows of 16)
+ *   conv_w, conv_b               [D][4], [D] float32
+ *   conv_state_in                NULL (zeros) or [B][3][conv_state_ld] float32, oldest first
+ *   ssm_state_in                 NULL (zeros) or [B][*][16] float32 with batch stride
+ *                                ssm_state_stride_b (>= 16*D), channel stride 16
+ *   conv_state_ld                row stride of conv_state_in/out, >= D
+ *   ssm_state_stride_b           batch stride of ssm_state_in/out, >= 16*D
+ *   out                          [B][L][D] view with out_stride_b, out_stride_t (>= D)
+ *   conv_state_out, ssm_state_out required, same layouts as the inputs; may not
+ *                                alias the inputs
+ * Returns SSM_OK or a negative status.
+ */
+int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                const void* x, const void* z, const void* dt,
+                int64_t in_stride_b, int64_t in_stride_t,
+                const void* Bmat, const void* Cmat,
+                const float* A, const float* Dskip, const float* dt_bias,
+                const float* conv_w, const float* conv_b,
+                const float* conv_state_in, const float* ssm_state_in,
+                int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                void* out, int64_t out_stride_b, int64_t out_stride_t,
+                float* conv_state_out, float* ssm_state_out,
+                void* cuda_stream);
+
+/*
+ * ssm_decode_step -- one token per request, continuing from cached states that
+ * are read and updated IN PLACE (Methodology 3: decode reuses the prefill state).
+ * Equals one more token of ssm_prefill.
+ *
+ *   batch                        number of requests (>= 1)
+ *   x, z, dt                     [batch][D] rows with row stride in_stride_b (>= D)
+ *   Bmat, Cmat                   [batch][16] contiguous
+ *   A .. conv_b                  as for ssm_prefill
+ *   conv_state                   [n_slots][3][conv_state_ld] float32, in/out
+ *   ssm_state                    [n_slots][*][16] float32, batch stride ssm_state_stride_b, in/out
+ *   state_slot                   NULL (request r uses slot r; needs n_slots >= batch) or a
+ *                                device array [batch] of slot indices; distinct requests must
+ *                                name distinct slots.  An index outside [0, n_slots) skips
+ *                                that request and sets SSM_DEV_BAD_SLOT in the status word.
+ *   out                          [batch][D] with row stride out_stride_b (>= D)
+ */
+int ssm_decode_step(int batch, int d_inner, int d_state, int d_conv,
+                    ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                    const void* x, const void* z, const void* dt, int64_t in_stride_b,
+                    const void* Bmat, const void* Cmat,
+                    const float* A, const float* Dskip, const float* dt_bias,
+                    const float* conv_w, const float* conv_b,
+                    float* conv_state, float* ssm_state,
+                    int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                    int n_slots, const int32_t* state_slot,
+                    void* out, int64_t out_stride_b,
+                    void* cuda_stream);
+
+/*
+ * q8_reduce_partials -- the arithmetic of the pages' 8-bit quantized all-reduce
+ * (Methodology 4), done locally over P partial buffers already in this GPU's
+ * memory: quantize every partial to int8 with one scale per block of `block`
+ * elements shared by all P partials (absolute maximum over the P partials / 127),
+ * sum the int8 codes in int32, dequantize the sum with that scale.
+ *
+ * Per block j:  amax = max_{p,i in j} |x_p[i]|;  if amax == 0: codes and scale are 0;
+ *   else inv = 127/amax and scale = amax/127 (IEEE fp32 division),
+ *   q_p[i] = round_half_even(x_p[i] * inv) clamped to [-127, 127],
+ *   S[i] = sum_p q_p[i] (int32),  out[i] = float(S[i]) * scale (fp32, then RNE to bf16
+ *   when out_dtype is bf16).  The last block may be shorter than `block`.
+ * Bit-exact: S and scale equal any IEEE-fp32 evaluation of the same steps, and
+ * |out - sum_p x_p| <= P*scale/2 plus fp32 rounding.
+ *
+ *   P                            1..8
+ *   partials                     HOST array of P device pointers, each to n elements of
+ *                                in_dtype, 16-byte aligned
+ *   n                            elements per partial (>= 1)
+ *   block                        must be 128
+ *   out                          [n] of out_dtype (device, 16-byte aligned)
+ *   sums_out                     NULL or [n] int32       scales_out  NULL or [ceil(n/block)]
+ */
+int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype, int64_t n,
+                       int block, void* out, ssm_dtype_t out_dtype, int32_t* sums_out,
+                       float* scales_out, void* cuda_stream);
+
+/*
+ * ssm_device_status -- read (and if `clear` is nonzero, reset) the device status
+ * word of the current device: an OR of SSM_DEV_* bits set by kernels that hit a
+ * bounded-wait timeout or a bad state slot since the last clear.  Synchronises
+ * the device.  Returns SSM_OK, or SSM_ERR_CUDA.
+ */
+int ssm_device_status(uint32_t* status, int clear);
+
+/* Thread-local text for the last non-OK return on this thread ("" if none). */
+const char* ssm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_H_ */

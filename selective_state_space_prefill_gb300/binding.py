@@ -1,0 +1,239 @@
+"""Thin ctypes binding over libssm (include/ssm.h): argument marshalling only.
+
+Every function takes CUDA torch tensors, checks their layouts, passes raw device
+pointers, element strides and the current torch stream to the C ABI, and raises
+``SSMError`` on a negative status.  All compute happens in libssm's kernels;
+there is no CPU or PyTorch fallback, and a missing library or device is an error.
+Output tensors are allocated with torch when the caller does not pass them.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+from .build import LIB
+
+SSM_F32, SSM_BF16 = 0, 1
+_STATUS = {0: "SSM_OK", -1: "SSM_ERR_INVALID_ARG", -2: "SSM_ERR_UNSUPPORTED", -3: "SSM_ERR_MISALIGNED",
+           -4: "SSM_ERR_CUDA", -5: "SSM_ERR_DEVICE_TIMEOUT"}
+DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
+
+EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_decode_step", "q8_reduce_partials",
+           "ssm_device_status", "ssm_last_error")
+
+
+class SSMError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} -> {_STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: Path | str | None = None):
+    """Load libssm.so (built by ``selective_state_space_prefill_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path else LIB
+    if not p.exists():
+        raise ImportError(f"libssm is not built ({p} missing): run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(str(p))
+    P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.ssm_abi_version.argtypes = []
+    lib.ssm_abi_version.restype = I
+    lib.ssm_last_error.argtypes = []
+    lib.ssm_last_error.restype = ctypes.c_char_p
+    lib.ssm_prefill.argtypes = [I, I, I, I, I, I, I, P, P, P, L, L, P, P, P, P, P, P, P, P, P, L, L,
+                                P, L, L, P, P, P]
+    lib.ssm_prefill.restype = I
+    lib.ssm_decode_step.argtypes = [I, I, I, I, I, I, P, P, P, L, P, P, P, P, P, P, P, P, P, L, L, I, P,
+                                    P, L, P]
+    lib.ssm_decode_step.restype = I
+    lib.q8_reduce_partials.argtypes = [I, P, I, L, I, P, I, P, P, P]
+    lib.q8_reduce_partials.restype = I
+    lib.ssm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
+    lib.ssm_device_status.restype = I
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(lib, fn: str, rc: int):
+    if rc != 0:
+        raise SSMError(fn, rc, lib.ssm_last_error().decode())
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return SSM_F32
+    if t == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported dtype {t} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libssm takes CUDA tensors only (no CPU path)")
+
+
+def _chan_contig(t, name):
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} must have channel stride 1")
+
+
+def _param(t, shape, name):
+    if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be contiguous float32 {tuple(shape)}")
+
+
+def _conv_state_layout(t, batch, d_inner, name):
+    if t.dtype != torch.float32 or tuple(t.shape) != (batch, 3, d_inner) or t.stride(2) != 1 \
+            or t.stride(0) != 3 * t.stride(1):
+        raise ValueError(f"{name} must be float32 [batch, 3, d_inner] with rows of one stride")
+    return t.stride(1)
+
+
+def _ssm_state_layout(t, batch, d_inner, name):
+    if t.dtype != torch.float32 or tuple(t.shape) != (batch, d_inner, 16) or t.stride(2) != 1 \
+            or t.stride(1) != 16:
+        raise ValueError(f"{name} must be float32 [batch, d_inner, 16] with channel stride 16")
+    return t.stride(0)
+
+
+def prefill(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state_in=None, ssm_state_in=None,
+            out=None, out_dtype=torch.float32, conv_state_out=None, ssm_state_out=None, stream=None):
+    """ssm_prefill over [batch, L, d_inner] x/z/dt (channel-stride-1 views allowed).
+
+    Returns (out, conv_state_out, ssm_state_out).
+    """
+    lib = load()
+    _need_cuda(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state_in, ssm_state_in)
+    batch, L, d_inner = x.shape
+    if z.shape != x.shape or dt.shape != x.shape or z.stride() != x.stride() or dt.stride() != x.stride():
+        raise ValueError("x, z, dt must share shape and strides")
+    if z.dtype != x.dtype or dt.dtype != x.dtype or B.dtype != x.dtype or C.dtype != x.dtype:
+        raise ValueError("x, z, dt, B, C must share one dtype")
+    for t, n in ((x, "x"),):
+        _chan_contig(t, n)
+    for t, n in ((B, "B"), (C, "C")):
+        if tuple(t.shape) != (batch, L, 16) or not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous [batch, L, 16]")
+    _param(A, (d_inner, 16), "A")
+    for t, n in ((D, "D"), (dt_bias, "dt_bias"), (conv_b, "conv_b")):
+        _param(t, (d_inner,), n)
+    _param(conv_w, (d_inner, 4), "conv_w")
+    dev = x.device
+    if out is None:
+        out = torch.empty(batch, L, d_inner, device=dev, dtype=out_dtype)
+    _chan_contig(out, "out")
+    if conv_state_out is None:
+        conv_state_out = torch.empty(batch, 3, d_inner, device=dev, dtype=torch.float32)
+    if ssm_state_out is None:
+        ssm_state_out = torch.empty(batch, d_inner, 16, device=dev, dtype=torch.float32)
+    ld = _conv_state_layout(conv_state_out, batch, d_inner, "conv_state_out")
+    sb = _ssm_state_layout(ssm_state_out, batch, d_inner, "ssm_state_out")
+    if conv_state_in is not None and _conv_state_layout(conv_state_in, batch, d_inner, "conv_state_in") != ld:
+        raise ValueError("conv_state_in and conv_state_out must share the row stride")
+    if ssm_state_in is not None and _ssm_state_layout(ssm_state_in, batch, d_inner, "ssm_state_in") != sb:
+        raise ValueError("ssm_state_in and ssm_state_out must share the batch stride")
+    rc = lib.ssm_prefill(batch, L, d_inner, 16, 4, _dtype_code(x.dtype), _dtype_code(out.dtype),
+                         _ptr(x), _ptr(z), _ptr(dt), x.stride(0), x.stride(1), _ptr(B), _ptr(C),
+                         _ptr(A), _ptr(D), _ptr(dt_bias), _ptr(conv_w), _ptr(conv_b),
+                         _ptr(conv_state_in), _ptr(ssm_state_in), ld, sb,
+                         _ptr(out), out.stride(0), out.stride(1),
+                         _ptr(conv_state_out), _ptr(ssm_state_out), _stream(stream))
+    _check(lib, "ssm_prefill", rc)
+    return out, conv_state_out, ssm_state_out
+
+
+def decode_step(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state, ssm_state, state_slot=None,
+                out=None, out_dtype=torch.float32, stream=None):
+    """ssm_decode_step: x/z/dt [batch, d_inner], B/C [batch, 16]; states updated in place.
+
+    conv_state [n_slots, 3, d_inner], ssm_state [n_slots, d_inner, 16] (channel-slice views allowed).
+    Returns out [batch, d_inner].
+    """
+    lib = load()
+    _need_cuda(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state, ssm_state, state_slot)
+    batch, d_inner = x.shape
+    if z.shape != x.shape or dt.shape != x.shape or z.stride() != x.stride() or dt.stride() != x.stride():
+        raise ValueError("x, z, dt must share shape and strides")
+    _chan_contig(x, "x")
+    for t, n in ((B, "B"), (C, "C")):
+        if tuple(t.shape) != (batch, 16) or not t.is_contiguous() or t.dtype != x.dtype:
+            raise ValueError(f"{n} must be contiguous [batch, 16] of the input dtype")
+    _param(A, (d_inner, 16), "A")
+    for t, n in ((D, "D"), (dt_bias, "dt_bias"), (conv_b, "conv_b")):
+        _param(t, (d_inner,), n)
+    _param(conv_w, (d_inner, 4), "conv_w")
+    n_slots = conv_state.shape[0]
+    if ssm_state.shape[0] != n_slots:
+        raise ValueError("conv_state and ssm_state must have the same number of slots")
+    ld = _conv_state_layout(conv_state, n_slots, d_inner, "conv_state")
+    sb = _ssm_state_layout(ssm_state, n_slots, d_inner, "ssm_state")
+    if state_slot is not None and (state_slot.dtype != torch.int32 or tuple(state_slot.shape) != (batch,)
+                                   or not state_slot.is_contiguous()):
+        raise ValueError("state_slot must be contiguous int32 [batch]")
+    if out is None:
+        out = torch.empty(batch, d_inner, device=x.device, dtype=out_dtype)
+    _chan_contig(out, "out")
+    rc = lib.ssm_decode_step(batch, d_inner, 16, 4, _dtype_code(x.dtype), _dtype_code(out.dtype),
+                             _ptr(x), _ptr(z), _ptr(dt), x.stride(0), _ptr(B), _ptr(C),
+                             _ptr(A), _ptr(D), _ptr(dt_bias), _ptr(conv_w), _ptr(conv_b),
+                             _ptr(conv_state), _ptr(ssm_state), ld, sb, n_slots, _ptr(state_slot),
+                             _ptr(out), out.stride(0), _stream(stream))
+    _check(lib, "ssm_decode_step", rc)
+    return out
+
+
+def q8_reduce(partials, block=128, out=None, out_dtype=None, sums=None, scales=None, stream=None):
+    """q8_reduce_partials over P equal-shaped partial tensors (flattened).
+
+    Returns (out, sums, scales); pass sums=False / scales=False to skip writing them.
+    """
+    lib = load()
+    _need_cuda(*partials)
+    P = len(partials)
+    shape, dtype = partials[0].shape, partials[0].dtype
+    for p in partials:
+        if p.shape != shape or p.dtype != dtype or not p.is_contiguous():
+            raise ValueError("partials must be contiguous tensors of one shape and dtype")
+    n = partials[0].numel()
+    dev = partials[0].device
+    out_dtype = out_dtype or dtype
+    if out is None:
+        out = torch.empty(shape, device=dev, dtype=out_dtype)
+    if sums is None:
+        sums = torch.empty(n, device=dev, dtype=torch.int32)
+    if scales is None:
+        scales = torch.empty((n + block - 1) // block, device=dev, dtype=torch.float32)
+    sums = sums if sums is not False else None
+    scales = scales if scales is not False else None
+    ptrs = (ctypes.c_void_p * P)(*[p.data_ptr() for p in partials])
+    rc = lib.q8_reduce_partials(P, ctypes.cast(ptrs, ctypes.c_void_p), _dtype_code(dtype), n, block,
+                                _ptr(out), _dtype_code(out.dtype), _ptr(sums), _ptr(scales), _stream(stream))
+    _check(lib, "q8_reduce_partials", rc)
+    return out, sums, scales
+
+
+def device_status(clear: bool = True) -> int:
+    """The device status word (OR of DEV_* bits); synchronises the device."""
+    lib = load()
+    v = ctypes.c_uint32(0)
+    _check(lib, "ssm_device_status", lib.ssm_device_status(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)

@@ -1,0 +1,261 @@
+// api.cu -- the extern "C" boundary of libssm (declared in include/ssm.h).
+//
+// Every entry point validates its arguments on the host, returns a negative
+// status (with a message for ssm_last_error) before launching anything when they
+// are wrong, and otherwise enqueues exactly one kernel on the caller's stream.
+// No entry point allocates memory or keeps per-call state.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/ssm.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+// Device status word: SSM_DEV_* bits OR-ed in by kernels.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+
+// Device address of the status word for the current device, looked up once per
+// device (with that device current) through cudaGetSymbolAddress.
+unsigned int* status_ptr(int* err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = 1;
+        return nullptr;
+    }
+    unsigned int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess || addr == nullptr) {
+        *err = 1;
+        return nullptr;
+    }
+    g_status_ptr[dev].store(static_cast<unsigned int*>(addr), std::memory_order_release);
+    return static_cast<unsigned int*>(addr);
+}
+
+bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool dtype_ok(int t) { return t == SSM_F32 || t == SSM_BF16; }
+int esize(int t) { return t == SSM_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+int ssm_abi_version(void) { return 100; }
+
+const char* ssm_last_error(void) { return g_err; }
+
+int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                const void* x, const void* z, const void* dt,
+                int64_t in_stride_b, int64_t in_stride_t,
+                const void* Bmat, const void* Cmat,
+                const float* A, const float* Dskip, const float* dt_bias,
+                const float* conv_w, const float* conv_b,
+                const float* conv_state_in, const float* ssm_state_in,
+                int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                void* out, int64_t out_stride_b, int64_t out_stride_t,
+                float* conv_state_out, float* ssm_state_out,
+                void* cuda_stream) {
+    g_err[0] = 0;
+    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: batch %lld not in [1, 65535]", (long long)(batch));
+    if (seqlen < 1 || seqlen > (1 << 30)) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: seqlen %lld not in [1, 2^30]", (long long)(seqlen));
+    if (d_inner < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: d_inner %lld < 1", (long long)(d_inner));
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: unknown dtype");
+    if (d_state != 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_prefill: d_state %lld unsupported (16 only)", (long long)(d_state));
+    if (d_conv != 4) return fail(SSM_ERR_UNSUPPORTED, "ssm_prefill: d_conv %lld unsupported (4 only)", (long long)(d_conv));
+    if (d_inner % 8 != 0) return fail(SSM_ERR_UNSUPPORTED, "ssm_prefill: d_inner %lld is not a multiple of 8", (long long)(d_inner));
+    if (!x || !z || !dt || !Bmat || !Cmat || !A || !Dskip || !dt_bias || !conv_w || !conv_b || !out ||
+        !conv_state_out || !ssm_state_out)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: a required pointer is NULL");
+    if (in_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: in_stride_t %lld < d_inner", (long long)(in_stride_t));
+    if (batch > 1 && in_stride_b < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: in_stride_b %lld < 1", (long long)(in_stride_b));
+    if (out_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: out_stride_t %lld < d_inner", (long long)(out_stride_t));
+    if (batch > 1 && out_stride_b < (int64_t)(seqlen - 1) * out_stride_t + d_inner)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: out_stride_b %lld lets batch rows overlap", (long long)(out_stride_b));
+    if (conv_state_ld < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: conv_state_ld %lld < d_inner", (long long)(conv_state_ld));
+    if (ssm_state_stride_b < 16LL * d_inner)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: ssm_state_stride_b %lld < 16*d_inner", (long long)(ssm_state_stride_b));
+    const int es = esize(in_dtype);
+    if (!aligned(x, 16) || !aligned(z, 16) || !aligned(dt, 16) || !aligned(Bmat, 16) || !aligned(Cmat, 16))
+        return fail(SSM_ERR_MISALIGNED, "ssm_prefill: x, z, dt, B and C must be 16-byte aligned");
+    if ((in_stride_t * es) % 16 != 0 || (batch > 1 && (in_stride_b * es) % 16 != 0))
+        return fail(SSM_ERR_MISALIGNED, "ssm_prefill: input strides must be multiples of 16 bytes");
+    if (!aligned(A, 16) || !aligned(conv_w, 16)) return fail(SSM_ERR_MISALIGNED, "ssm_prefill: A and conv_w must be 16-byte aligned");
+    if (!aligned(ssm_state_out, 8) || (ssm_state_in && !aligned(ssm_state_in, 8)) || ssm_state_stride_b % 2 != 0)
+        return fail(SSM_ERR_MISALIGNED, "ssm_prefill: ssm states must be 8-byte aligned with an even batch stride");
+    if (!aligned(out, esize(out_dtype))) return fail(SSM_ERR_MISALIGNED, "ssm_prefill: out is not element aligned");
+
+    int serr = 0;
+    unsigned int* status = status_ptr(&serr);
+    if (serr) return fail(SSM_ERR_CUDA, "ssm_prefill: no usable CUDA device");
+
+    ssm::PrefillLaunch q{};
+    q.batch = batch;
+    q.in_bf16 = in_dtype == SSM_BF16;
+    q.out_bf16 = out_dtype == SSM_BF16;
+    q.z = z;
+    q.dt = dt;
+    q.Bm = Bmat;
+    q.Cm = Cmat;
+    ssm::PrefillArgs& a = q.args;
+    a.seqlen = seqlen;
+    a.d_inner = d_inner;
+    a.x = x;
+    a.in_stride_b = in_stride_b;
+    a.in_stride_t = in_stride_t;
+    a.A = A;
+    a.Dskip = Dskip;
+    a.dt_bias = dt_bias;
+    a.conv_w = conv_w;
+    a.conv_b = conv_b;
+    a.conv_state_in = conv_state_in;
+    a.ssm_state_in = ssm_state_in;
+    a.conv_state_ld = conv_state_ld;
+    a.ssm_state_stride_b = ssm_state_stride_b;
+    a.out = out;
+    a.out_stride_b = out_stride_b;
+    a.out_stride_t = out_stride_t;
+    a.conv_state_out = conv_state_out;
+    a.ssm_state_out = ssm_state_out;
+    a.status = status;
+    const char* why = "";
+    if (ssm::launch_prefill(q, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "ssm_prefill: %s", why);
+    return SSM_OK;
+}
+
+int ssm_decode_step(int batch, int d_inner, int d_state, int d_conv,
+                    ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                    const void* x, const void* z, const void* dt, int64_t in_stride_b,
+                    const void* Bmat, const void* Cmat,
+                    const float* A, const float* Dskip, const float* dt_bias,
+                    const float* conv_w, const float* conv_b,
+                    float* conv_state, float* ssm_state,
+                    int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                    int n_slots, const int32_t* state_slot,
+                    void* out, int64_t out_stride_b,
+                    void* cuda_stream) {
+    g_err[0] = 0;
+    if (batch < 1 || batch > (1 << 24)) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: batch %lld out of range", (long long)(batch));
+    if (d_inner < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: d_inner %lld < 1", (long long)(d_inner));
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: unknown dtype");
+    if (d_state != 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_decode_step: d_state %lld unsupported (16 only)", (long long)(d_state));
+    if (d_conv != 4) return fail(SSM_ERR_UNSUPPORTED, "ssm_decode_step: d_conv %lld unsupported (4 only)", (long long)(d_conv));
+    if (d_inner % 8 != 0) return fail(SSM_ERR_UNSUPPORTED, "ssm_decode_step: d_inner %lld is not a multiple of 8", (long long)(d_inner));
+    if (!x || !z || !dt || !Bmat || !Cmat || !A || !Dskip || !dt_bias || !conv_w || !conv_b || !conv_state ||
+        !ssm_state || !out)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: a required pointer is NULL");
+    if (in_stride_b < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: in_stride_b %lld < d_inner", (long long)(in_stride_b));
+    if (out_stride_b < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: out_stride_b %lld < d_inner", (long long)(out_stride_b));
+    if (conv_state_ld < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: conv_state_ld %lld < d_inner", (long long)(conv_state_ld));
+    if (ssm_state_stride_b < 16LL * d_inner)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: ssm_state_stride_b %lld < 16*d_inner", (long long)(ssm_state_stride_b));
+    if (n_slots < 1 || (!state_slot && n_slots < batch))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: n_slots %lld too small", (long long)(n_slots));
+    const int es = esize(in_dtype);
+    if (!aligned(Bmat, 4 * es) || !aligned(Cmat, 4 * es))
+        return fail(SSM_ERR_MISALIGNED, "ssm_decode_step: B and C must be aligned to 4 elements");
+    if (!aligned(A, 16) || !aligned(conv_w, 16) || !aligned(ssm_state, 16) || ssm_state_stride_b % 4 != 0)
+        return fail(SSM_ERR_MISALIGNED, "ssm_decode_step: A, conv_w and ssm_state need 16-byte alignment");
+    if (!aligned(x, es) || !aligned(z, es) || !aligned(dt, es) || !aligned(out, esize(out_dtype)) ||
+        !aligned(conv_state, 4) || (state_slot && !aligned(state_slot, 4)))
+        return fail(SSM_ERR_MISALIGNED, "ssm_decode_step: a pointer is not element aligned");
+
+    int serr = 0;
+    unsigned int* status = status_ptr(&serr);
+    if (serr) return fail(SSM_ERR_CUDA, "ssm_decode_step: no usable CUDA device");
+
+    ssm::DecodeArgs a{};
+    a.batch = batch;
+    a.d_inner = d_inner;
+    a.n_slots = n_slots;
+    a.x = x;
+    a.z = z;
+    a.dt = dt;
+    a.in_stride_b = in_stride_b;
+    a.Bm = Bmat;
+    a.Cm = Cmat;
+    a.A = A;
+    a.Dskip = Dskip;
+    a.dt_bias = dt_bias;
+    a.conv_w = conv_w;
+    a.conv_b = conv_b;
+    a.conv_state = conv_state;
+    a.ssm_state = ssm_state;
+    a.conv_state_ld = conv_state_ld;
+    a.ssm_state_stride_b = ssm_state_stride_b;
+    a.state_slot = state_slot;
+    a.out = out;
+    a.out_stride_b = out_stride_b;
+    a.status = status;
+    const char* why = "";
+    if (ssm::launch_decode(a, in_dtype == SSM_BF16, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream),
+                           &why) != 0)
+        return fail(SSM_ERR_CUDA, "ssm_decode_step: %s", why);
+    return SSM_OK;
+}
+
+int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype, int64_t n, int block,
+                       void* out, ssm_dtype_t out_dtype, int32_t* sums_out, float* scales_out,
+                       void* cuda_stream) {
+    g_err[0] = 0;
+    if (P < 1 || P > ssm::kMaxPartials) return fail(SSM_ERR_UNSUPPORTED, "q8_reduce_partials: P %lld not in [1, 8]", (long long)(P));
+    if (!partials) return fail(SSM_ERR_INVALID_ARG, "q8_reduce_partials: partials is NULL");
+    if (n < 1) return fail(SSM_ERR_INVALID_ARG, "q8_reduce_partials: n %lld < 1", (long long)(n));
+    if (block != 128) return fail(SSM_ERR_UNSUPPORTED, "q8_reduce_partials: block %lld unsupported (128 only)", (long long)(block));
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "q8_reduce_partials: unknown dtype");
+    if (!out) return fail(SSM_ERR_INVALID_ARG, "q8_reduce_partials: out is NULL");
+    ssm::Q8Args a{};
+    for (int p = 0; p < P; ++p) {
+        if (!partials[p]) return fail(SSM_ERR_INVALID_ARG, "q8_reduce_partials: partials[%lld] is NULL", (long long)(p));
+        if (!aligned(partials[p], 16)) return fail(SSM_ERR_MISALIGNED, "q8_reduce_partials: partials[%lld] not 16-byte aligned", (long long)(p));
+        a.partials[p] = partials[p];
+    }
+    if (!aligned(out, 16) || (sums_out && !aligned(sums_out, 16)) || (scales_out && !aligned(scales_out, 4)))
+        return fail(SSM_ERR_MISALIGNED, "q8_reduce_partials: out and sums must be 16-byte aligned");
+    a.P = P;
+    a.n = n;
+    a.out = out;
+    a.sums = sums_out;
+    a.scales = scales_out;
+    const char* why = "";
+    if (ssm::launch_q8(a, in_dtype == SSM_BF16, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "q8_reduce_partials: %s", why);
+    return SSM_OK;
+}
+
+int ssm_device_status(uint32_t* status, int clear) {
+    g_err[0] = 0;
+    if (!status) return fail(SSM_ERR_INVALID_ARG, "ssm_device_status: status is NULL");
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof v) != cudaSuccess)
+        return fail(SSM_ERR_CUDA, "ssm_device_status: cudaMemcpyFromSymbol failed");
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess)
+            return fail(SSM_ERR_CUDA, "ssm_device_status: cudaMemcpyToSymbol failed");
+    }
+    *status = v;
+    return SSM_OK;
+}
+
+}  // extern "C"

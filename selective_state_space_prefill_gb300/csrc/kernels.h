@@ -1,0 +1,63 @@
+// kernels.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/ssm.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssm {
+
+// Kernel-side arguments of the prefill (everything except the TMA maps).
+struct PrefillArgs {
+    int seqlen, d_inner;
+    const void* x;                  // raw x, for the final conv state
+    int64_t in_stride_b, in_stride_t;
+    const float *A, *Dskip, *dt_bias, *conv_w, *conv_b;
+    const float *conv_state_in, *ssm_state_in;
+    int64_t conv_state_ld, ssm_state_stride_b;
+    void* out;
+    int64_t out_stride_b, out_stride_t;
+    float *conv_state_out, *ssm_state_out;
+    unsigned int* status;
+};
+
+struct PrefillLaunch {
+    int batch;
+    bool in_bf16, out_bf16;
+    const void *z, *dt, *Bm, *Cm;
+    PrefillArgs args;
+};
+
+struct DecodeArgs {
+    int batch, d_inner, n_slots;
+    const void *x, *z, *dt;
+    int64_t in_stride_b;
+    const void *Bm, *Cm;
+    const float *A, *Dskip, *dt_bias, *conv_w, *conv_b;
+    float *conv_state, *ssm_state;
+    int64_t conv_state_ld, ssm_state_stride_b;
+    const int32_t* state_slot;
+    void* out;
+    int64_t out_stride_b;
+    unsigned int* status;
+};
+
+constexpr int kMaxPartials = 8;
+
+struct Q8Args {
+    const void* partials[kMaxPartials];
+    int P;
+    int64_t n;
+    void* out;
+    int32_t* sums;
+    float* scales;
+};
+
+// Each returns 0 on success, or -1 with *why set to a static message.
+int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why);
+int launch_decode(const DecodeArgs& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
+int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
+
+int prefill_chunk_tokens();
+
+}  // namespace ssm

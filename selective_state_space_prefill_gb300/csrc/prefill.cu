@@ -1,0 +1,399 @@
+// prefill.cu -- selective-SSM prefill on sm_103a.
+//
+// Computes, for every batch row b, channel d and token t (N = 16 states, conv width 4),
+//   u_t = SiLU(conv_b + sum_k conv_w[k] x_{t-3+k}),  delta_t = softplus(dt_t + dt_bias),
+//   h_t[n] = exp(delta_t A[n]) h_{t-1}[n] + delta_t B_t[n] u_t,
+//   out_t = (sum_n C_t[n] h_t[n] + D u_t) * SiLU(z_t),
+// and the final conv and SSM states.  The recurrence never leaves its channel
+// ("Scaling State-Space Models on Multiple GPUs with Tensor Parallelism",
+// Methodology 2, local recurrence) and the final states are the cache that
+// decode continues from (Methodology 3).
+//
+// Design (one GB300, HBM- and ALU-bound; no tensor cores: the recurrence is
+// diagonal, not a contraction):
+//   * One CTA owns 32 channels (one per lane) of one batch row for the WHOLE
+//     sequence, so the carry between time chunks stays in registers: no
+//     scratch memory, no inter-CTA waits, one launch.
+//   * Time advances in chunks of TC = S*K tokens.  Warp j of the S warps owns the
+//     K consecutive tokens [j*K, j*K + K) of the chunk; inside a warp every lane
+//     runs the same tokens for its own channel, so B_t/C_t reads are shared-memory
+//     broadcasts and x/z/dt/out accesses are 32 consecutive channels.
+//   * Staging: a 3-stage ring of TMA tile copies (x with a 3-token conv halo,
+//     z, dt as [TC x 32] boxes; B, C as [TC x 16] boxes) completing on mbarriers,
+//     issued one chunk ahead by one thread.  Out-of-range rows/channels arrive
+//     as zeros.
+//   * The scan is a chunked associative scan of (a, b) pairs, two states at a
+//     time in packed f32x2 arithmetic:
+//       1. per lane, a_i = 2^(delta_i A'[n]), b_i = delta_i u_i B_i[n] for its K
+//          tokens and the sub-chunk aggregate (prod a, folded b) -- the product
+//          of the a_i is taken as 2^(A'[n] * sum delta_i);
+//       2. the S sub-chunk aggregates meet in shared memory; each warp folds the
+//          ones before it onto the carried-in chunk state to get its start state,
+//          and every warp folds all S to get the next chunk's carry;
+//       3. each lane replays its K tokens from the start state and accumulates
+//          y_i += C_i[n] h_i[n].
+//   * The split of the work depends only on the compile-time S and K, never on
+//     d_inner, the grid or occupancy, so a channel's result is bit-identical
+//     whatever channel slice it is computed in.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ssm {
+
+namespace {
+
+constexpr int kCD = 32;      // channels per CTA (one per lane)
+constexpr int kN = 16;       // d_state
+constexpr int kStages = 3;   // TMA ring depth
+
+constexpr int align128(int v) { return (v + 127) / 128 * 128; }
+
+template <int S, int K, typename Tin>
+struct Layout {
+    static constexpr int TC = S * K;
+    static constexpr int XROWS = TC + 3;
+    static constexpr int ES = (int)sizeof(Tin);
+    static constexpr int X_BYTES = XROWS * kCD * ES;
+    static constexpr int Z_BYTES = TC * kCD * ES;
+    static constexpr int BC_BYTES = TC * kN * ES;
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_Z = align128(OFF_X + X_BYTES);
+    static constexpr int OFF_DT = align128(OFF_Z + Z_BYTES);
+    static constexpr int OFF_B = align128(OFF_DT + Z_BYTES);
+    static constexpr int OFF_C = align128(OFF_B + BC_BYTES);
+    static constexpr int STAGE = align128(OFF_C + BC_BYTES);
+    static constexpr int TX = X_BYTES + 2 * Z_BYTES + 2 * BC_BYTES;   // bytes per stage fill
+    // after the ring: fp32 copies of B and C for the chunk, the exchange slots, barriers
+    static constexpr int OFF_BF = kStages * STAGE;
+    static constexpr int OFF_CF = OFF_BF + TC * kN * 4;
+    static constexpr int OFF_XCH = OFF_CF + TC * kN * 4;
+    static constexpr int XCH_BYTES = 2 * S * 32 * 16;
+    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    static constexpr int TOTAL = OFF_BAR + kStages * 8;
+};
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+template <int S, int K, typename Tin, typename Tout>
+__global__ void __launch_bounds__(S * 32, 1)
+k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
+          const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_B,
+          const __grid_constant__ CUtensorMap tm_C, const PrefillArgs p) {
+    using Lay = Layout<S, K, Tin>;
+    constexpr int TC = Lay::TC;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* Bf = reinterpret_cast<float*>(smem + Lay::OFF_BF);
+    float* Cf = reinterpret_cast<float*>(smem + Lay::OFF_CF);
+    float4* xch = reinterpret_cast<float4*>(smem + Lay::OFF_XCH);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::OFF_BAR);
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int d0 = blockIdx.x * kCD;
+    const int b = blockIdx.y;
+    const int d = d0 + lane;
+    const bool dvalid = d < p.d_inner;
+    const int L = p.seqlen;
+    const int n_iter = (L + TC - 1) / TC;
+
+    // TMA destinations need 128-byte alignment; refuse (and report) rather than fault.
+    if (smem_u32(smem) & 127u) {
+        if (threadIdx.x == 0) atomicOr(p.status, 4u);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_z);
+        prefetch_tmap(&tm_dt);
+        prefetch_tmap(&tm_B);
+        prefetch_tmap(&tm_C);
+    }
+    __syncthreads();
+
+    auto issue = [&](int it) {
+        const int s = it % kStages;
+        unsigned char* st = smem + s * Lay::STAGE;
+        const int t0 = it * TC;
+        mbar_arrive_expect_tx(&full[s], Lay::TX);
+        tma_load_3d(st + Lay::OFF_X, &tm_x, &full[s], d0, t0 - 3, b);
+        tma_load_3d(st + Lay::OFF_Z, &tm_z, &full[s], d0, t0, b);
+        tma_load_3d(st + Lay::OFF_DT, &tm_dt, &full[s], d0, t0, b);
+        tma_load_3d(st + Lay::OFF_B, &tm_B, &full[s], 0, t0, b);
+        tma_load_3d(st + Lay::OFF_C, &tm_C, &full[s], 0, t0, b);
+    };
+    if (threadIdx.x == 0) {
+        for (int it = 0; it < kStages - 1 && it < n_iter; ++it) issue(it);
+    }
+
+    // ---- per-channel parameters (zeros for channels past d_inner)
+    float A2[kN];   // A * log2(e): exp(delta A) = 2^(delta A2)
+    float Dd = 0.f, bias = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f, cb = 0.f;
+    float2 carry[kN / 2];
+#pragma unroll
+    for (int n = 0; n < kN; ++n) A2[n] = 0.f;
+#pragma unroll
+    for (int q = 0; q < kN / 2; ++q) carry[q] = f2(0.f, 0.f);
+    if (dvalid) {
+        const float4* Ar = reinterpret_cast<const float4*>(p.A + (int64_t)d * kN);
+#pragma unroll
+        for (int q = 0; q < kN / 4; ++q) {
+            const float4 v = __ldg(Ar + q);
+            A2[4 * q + 0] = v.x * kLog2e;
+            A2[4 * q + 1] = v.y * kLog2e;
+            A2[4 * q + 2] = v.z * kLog2e;
+            A2[4 * q + 3] = v.w * kLog2e;
+        }
+        const float4 w = __ldg(reinterpret_cast<const float4*>(p.conv_w + (int64_t)d * 4));
+        w0 = w.x; w1 = w.y; w2 = w.z; w3 = w.w;
+        cb = __ldg(p.conv_b + d);
+        Dd = __ldg(p.Dskip + d);
+        bias = __ldg(p.dt_bias + d);
+        if (p.ssm_state_in) {
+            const float2* hs = reinterpret_cast<const float2*>(
+                p.ssm_state_in + (int64_t)b * p.ssm_state_stride_b + (int64_t)d * kN);
+#pragma unroll
+            for (int q = 0; q < kN / 2; ++q) carry[q] = hs[q];
+        }
+    }
+
+    for (int it = 0; it < n_iter; ++it) {
+        const int s = it % kStages;
+        const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((it / kStages) & 1));
+        if (__syncthreads_or(!ok)) {
+            // A copy never completed: record it, let every issued copy land (bounded) and stop.
+            if (threadIdx.x == 0) {
+                atomicOr(p.status, 1u);
+                for (int j = it; j < n_iter && j < it + kStages - 1; ++j)
+                    (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1),
+                                            100000000ull);
+            }
+            return;
+        }
+        const unsigned char* st = smem + s * Lay::STAGE;
+        const Tin* xs = reinterpret_cast<const Tin*>(st + Lay::OFF_X);
+        const Tin* zs = reinterpret_cast<const Tin*>(st + Lay::OFF_Z);
+        const Tin* dts = reinterpret_cast<const Tin*>(st + Lay::OFF_DT);
+        const Tin* Bs = reinterpret_cast<const Tin*>(st + Lay::OFF_B);
+        const Tin* Cs = reinterpret_cast<const Tin*>(st + Lay::OFF_C);
+
+        // ---- this warp's K rows of B and C, widened to fp32 once
+        {
+            float* bw = Bf + warp * K * kN;
+            float* cw = Cf + warp * K * kN;
+            const Tin* bsrc = Bs + warp * K * kN;
+            const Tin* csrc = Cs + warp * K * kN;
+#pragma unroll
+            for (int e = lane; e < K * kN; e += 32) {
+                bw[e] = to_f32(bsrc[e]);
+                cw[e] = to_f32(csrc[e]);
+            }
+            __syncwarp();
+        }
+
+        // ---- pointwise: conv + SiLU, softplus step, skip term
+        const int row0 = warp * K;            // first token of this warp in the chunk
+        const int tbase = it * TC + row0;     // its absolute index
+        float xm3 = to_f32(xs[(row0 + 0) * kCD + lane]);   // x[tbase-3]  (tile row 0 = chunk start - 3)
+        float xm2 = to_f32(xs[(row0 + 1) * kCD + lane]);
+        float xm1 = to_f32(xs[(row0 + 2) * kCD + lane]);
+        if (it == 0 && warp == 0 && p.conv_state_in != nullptr && dvalid) {
+            const float* cs = p.conv_state_in + (int64_t)b * 3 * p.conv_state_ld + d;
+            xm3 = cs[0];
+            xm2 = cs[p.conv_state_ld];
+            xm1 = cs[2 * p.conv_state_ld];
+        }
+        float dl[K], du[K], y[K];
+        float dsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const float xt = to_f32(xs[(row0 + i + 3) * kCD + lane]);
+            float xc = fmaf(w0, xm3, cb);
+            xc = fmaf(w1, xm2, xc);
+            xc = fmaf(w2, xm1, xc);
+            xc = fmaf(w3, xt, xc);
+            xm3 = xm2; xm2 = xm1; xm1 = xt;
+            const float u = silu(xc);
+            float delta = softplus(to_f32(dts[(row0 + i) * kCD + lane]) + bias);
+            if (tbase + i >= L) delta = 0.f;   // padding rows: a = 1, b = 0 (identity)
+            dl[i] = delta;
+            du[i] = delta * u;
+            y[i] = Dd * u;
+            dsum += delta;
+        }
+
+        // ---- the scan, two states at a time
+        const float* bw = Bf + warp * K * kN;
+        const float* cw = Cf + warp * K * kN;
+#pragma unroll
+        for (int pr = 0; pr < kN / 2; ++pr) {
+            const float2 Ap = f2(A2[2 * pr], A2[2 * pr + 1]);
+            float2 a[K], bb[K];
+            float2 agg = f2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const float2 e = __fmul2_rn(f2(dl[i], dl[i]), Ap);
+                a[i] = f2(ex2(e.x), ex2(e.y));
+                const float2 Bi = *reinterpret_cast<const float2*>(bw + i * kN + 2 * pr);
+                bb[i] = __fmul2_rn(f2(du[i], du[i]), Bi);
+                agg = __ffma2_rn(a[i], agg, bb[i]);
+            }
+            const float2 ea = __fmul2_rn(f2(dsum, dsum), Ap);
+            xch[((pr & 1) * S + warp) * 32 + lane] = make_float4(ex2(ea.x), ex2(ea.y), agg.x, agg.y);
+            __syncthreads();
+            if (pr == 0 && threadIdx.x == 0 && it + kStages - 1 < n_iter) {
+                // every warp has finished chunk it-1, so its stage can be refilled
+                issue(it + kStages - 1);
+            }
+            float2 h = carry[pr], hs = h;
+#pragma unroll
+            for (int j = 0; j < S; ++j) {
+                const float4 e = xch[((pr & 1) * S + j) * 32 + lane];
+                if (j == warp) hs = h;
+                h = __ffma2_rn(f2(e.x, e.y), h, f2(e.z, e.w));
+            }
+            carry[pr] = h;
+            h = hs;
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                h = __ffma2_rn(a[i], h, bb[i]);
+                const float2 Ci = *reinterpret_cast<const float2*>(cw + i * kN + 2 * pr);
+                y[i] = fmaf(Ci.x, h.x, fmaf(Ci.y, h.y, y[i]));
+            }
+        }
+
+        // ---- gate and store
+        if (dvalid) {
+            Tout* o = reinterpret_cast<Tout*>(p.out) + (int64_t)b * p.out_stride_b + d;
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const int t = tbase + i;
+                if (t < L) {
+                    const float g = silu(to_f32(zs[(row0 + i) * kCD + lane]));
+                    o[(int64_t)t * p.out_stride_t] = from_f32<Tout>(y[i] * g);
+                }
+            }
+        }
+    }
+
+    // ---- final states: h_L and the last three raw inputs
+    if (warp == 0 && dvalid) {
+        float2* hs = reinterpret_cast<float2*>(p.ssm_state_out + (int64_t)b * p.ssm_state_stride_b +
+                                               (int64_t)d * kN);
+#pragma unroll
+        for (int q = 0; q < kN / 2; ++q) hs[q] = carry[q];
+        const Tin* xg = reinterpret_cast<const Tin*>(p.x) + (int64_t)b * p.in_stride_b + d;
+        float* co = p.conv_state_out + (int64_t)b * 3 * p.conv_state_ld + d;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int t = L - 3 + k;
+            float v = 0.f;
+            if (t >= 0) {
+                v = to_f32(xg[(int64_t)t * p.in_stride_t]);
+            } else if (p.conv_state_in != nullptr) {
+                v = p.conv_state_in[(int64_t)b * 3 * p.conv_state_ld + (int64_t)(t + 3) * p.conv_state_ld + d];
+            }
+            co[(int64_t)k * p.conv_state_ld] = v;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3-D map over [dim2][dim1][dim0] elements with byte strides s1 (dim1) and s2 (dim2).
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t dim0,
+              uint64_t dim1, uint64_t dim2, uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {dim0, dim1, dim2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    (void)esize;
+    CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int S, int K, typename Tin, typename Tout>
+int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
+    using Lay = Layout<S, K, Tin>;
+    constexpr int TC = Lay::TC;
+    const int es = (int)sizeof(Tin);
+    const CUtensorMapDataType dt =
+        sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const PrefillArgs& a = q.args;
+    const uint64_t sb = (uint64_t)(q.batch > 1 ? a.in_stride_b : (int64_t)a.seqlen * a.in_stride_t) * es;
+    const uint64_t st = (uint64_t)a.in_stride_t * es;
+    const uint64_t bc_t = (uint64_t)kN * es, bc_b = (uint64_t)a.seqlen * kN * es;
+    CUtensorMap mx, mz, mdt, mB, mC;
+    if (!make_map(&mx, a.x, dt, es, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC + 3) ||
+        !make_map(&mz, q.z, dt, es, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
+        !make_map(&mdt, q.dt, dt, es, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
+        !make_map(&mB, q.Bm, dt, es, kN, a.seqlen, q.batch, bc_t, bc_b, kN, TC) ||
+        !make_map(&mC, q.Cm, dt, es, kN, a.seqlen, q.batch, bc_t, bc_b, kN, TC)) {
+        *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
+        return -1;
+    }
+    auto kern = k_prefill<S, K, Tin, Tout>;
+    // The shared-memory opt-in is per function and device; remember it per device.
+    static unsigned long long attr_done = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        *why = "cudaGetDevice failed";
+        return -1;
+    }
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL) !=
+            cudaSuccess) {
+            *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+            return -1;
+        }
+        __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
+    }
+    dim3 grid((a.d_inner + kCD - 1) / kCD, q.batch);
+    kern<<<grid, S * 32, Lay::TOTAL, stream>>>(mx, mz, mdt, mB, mC, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return -1;
+    }
+    return 0;
+}
+
+}  // namespace
+
+// Compile-time split of a chunk: S warps x K tokens.
+constexpr int kS = 4;
+constexpr int kK = 16;
+
+int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
+    if (q.in_bf16) {
+        return q.out_bf16 ? launch_t<kS, kK, __nv_bfloat16, __nv_bfloat16>(q, stream, why)
+                          : launch_t<kS, kK, __nv_bfloat16, float>(q, stream, why);
+    }
+    return q.out_bf16 ? launch_t<kS, kK, float, __nv_bfloat16>(q, stream, why)
+                      : launch_t<kS, kK, float, float>(q, stream, why);
+}
+
+int prefill_chunk_tokens() { return kS * kK; }
+
+}  // namespace ssm

@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+* libssm.so builds for sm_103a and exports every function include/ssm.h declares;
+* argument validation returns the documented status before any CUDA call
+  (pointers here are fake and never dereferenced: every call is rejected first).
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from selective_state_space_prefill_gb300 import binding, build
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "ssm.h"
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA = 0, -1, -2, -3, -4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"^(?:int|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for fn in ("ssm_prefill", "ssm_decode_step", "q8_reduce_partials"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(binding.EXPORTS)
+    for fn in names:
+        assert hasattr(lib, fn), fn
+    assert lib.ssm_abi_version() == 100
+
+
+FAKE = 0x10000  # 64 KiB-aligned fake device address, never dereferenced
+
+
+def _prefill(lib, **kw):
+    a = dict(batch=2, seqlen=16, d_inner=64, d_state=16, d_conv=4, in_dtype=1, out_dtype=0,
+             x=FAKE, z=FAKE, dt=FAKE, in_stride_b=16 * 64, in_stride_t=64, B=FAKE, C=FAKE, A=FAKE,
+             D=FAKE, dt_bias=FAKE, conv_w=FAKE, conv_b=FAKE, csi=None, ssi=None, ld=64, sb=64 * 16,
+             out=FAKE, ob=16 * 64, ot=64, cso=FAKE, sso=FAKE, stream=None)
+    a.update(kw)
+    return lib.ssm_prefill(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=0), INVALID), (dict(seqlen=0), INVALID), (dict(d_inner=0), INVALID),
+    (dict(in_dtype=7), INVALID), (dict(d_state=8), UNSUPPORTED), (dict(d_conv=3), UNSUPPORTED),
+    (dict(d_inner=60, in_stride_t=60, ld=60, sb=960), UNSUPPORTED), (dict(x=None), INVALID),
+    (dict(sso=None), INVALID), (dict(in_stride_t=32), INVALID), (dict(ob=64), INVALID),
+    (dict(ld=32), INVALID), (dict(sb=100), INVALID), (dict(x=FAKE + 8), MISALIGNED),
+    (dict(in_stride_t=68), MISALIGNED), (dict(A=FAKE + 4), MISALIGNED), (dict(sso=FAKE + 4), MISALIGNED),
+])
+def test_prefill_rejects_bad_arguments(lib, kw, code):
+    assert _prefill(lib, **kw) == code
+    assert lib.ssm_last_error().decode().startswith("ssm_prefill")
+
+
+def _decode(lib, **kw):
+    a = dict(batch=4, d_inner=64, d_state=16, d_conv=4, in_dtype=1, out_dtype=0, x=FAKE, z=FAKE,
+             dt=FAKE, sx=64, B=FAKE, C=FAKE, A=FAKE, D=FAKE, dt_bias=FAKE, conv_w=FAKE, conv_b=FAKE,
+             cs=FAKE, ss=FAKE, ld=64, sb=1024, n_slots=4, slot=None, out=FAKE, so=64, stream=None)
+    a.update(kw)
+    return lib.ssm_decode_step(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=0), INVALID), (dict(d_state=32), UNSUPPORTED), (dict(cs=None), INVALID),
+    (dict(n_slots=2), INVALID), (dict(sx=32), INVALID), (dict(ss=FAKE + 8), MISALIGNED),
+    (dict(B=FAKE + 2), MISALIGNED),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def _q8(lib, P=4, ptrs=None, **kw):
+    arr = (ctypes.c_void_p * max(P, 1))(*(ptrs or [FAKE] * max(P, 1)))
+    a = dict(P=P, partials=ctypes.cast(arr, ctypes.c_void_p), dtype=1, n=4096, block=128, out=FAKE,
+             out_dtype=1, sums=None, scales=None, stream=None)
+    a.update(kw)
+    return lib.q8_reduce_partials(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(P=0), UNSUPPORTED), (dict(P=9), UNSUPPORTED), (dict(n=0), INVALID), (dict(block=64), UNSUPPORTED),
+    (dict(out=None), INVALID), (dict(ptrs=[FAKE, FAKE + 8, FAKE, FAKE]), MISALIGNED),
+    (dict(partials=None), INVALID),
+])
+def test_q8_rejects_bad_arguments(lib, kw, code):
+    assert _q8(lib, **kw) == code
+
+
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    """A well-formed call on a machine without a usable GPU returns SSM_ERR_CUDA, not a crash."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _prefill(lib) == CUDA

@@ -1,0 +1,118 @@
+"""ssm_prefill on the GPU against the fp64 oracle, element by element (small and ragged cases)."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from _gpu import (assert_rms_close, cpu_channels, half_ulp_bf16, oracle_prefill, run_prefill, tol_for)
+from selective_state_space_prefill_gb300 import binding as ssm
+from selective_state_space_prefill_gb300.inputs import make_mixer_inputs, make_states
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+CASES = [
+    # name, batch, L, d_inner, dtype, with input states
+    ("tiny_fp32_L256", 1, 256, 64, torch.float32, False),
+    ("tiny_fp32_L192", 1, 192, 64, torch.float32, False),
+    ("ragged_bf16_states", 2, 300, 72, torch.bfloat16, True),
+    ("ragged_fp32_states", 3, 130, 40, torch.float32, True),
+    ("L1_states", 2, 1, 32, torch.bfloat16, True),
+    ("L2_states", 1, 2, 64, torch.float32, True),
+    ("L3", 1, 3, 64, torch.float32, False),
+    ("one_chunk", 1, 64, 96, torch.bfloat16, False),
+    ("chunk_plus_one", 2, 65, 96, torch.bfloat16, True),
+    ("two_chunks", 1, 128, 128, torch.float32, True),
+    ("d_inner_8", 2, 77, 8, torch.bfloat16, True),
+    ("many_chunks", 1, 1000, 64, torch.bfloat16, False),
+]
+
+
+@pytest.mark.parametrize("name,batch,L,D,dtype,states", CASES, ids=[c[0] for c in CASES])
+def test_prefill_matches_oracle(name, batch, L, D, dtype, states):
+    inp = make_mixer_inputs(batch, L, D, dtype=dtype, seed=zlib.crc32(name.encode()) % 1000)
+    cs = ss = None
+    if states:
+        cs, ss = make_states(batch, D, seed=7)
+    g = inp.to(DEV)
+    out, cso, sso = run_prefill(g, None if cs is None else cs.to(DEV), None if ss is None else ss.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle_prefill(inp, cs, ss)
+    tol = tol_for(dtype)
+    assert_rms_close(out, ref["out"], tol, "out")
+    assert_rms_close(sso, ref["ssm_state"], tol, "ssm_state")
+    assert np.array_equal(cso.cpu().double().numpy(), ref["conv_state"]), "conv_state must be exact"
+    assert ssm.device_status() == 0
+
+
+def test_prefill_bf16_output():
+    inp = make_mixer_inputs(2, 257, 64, dtype=torch.bfloat16, seed=5)
+    out, _, _ = run_prefill(inp.to(DEV), out_dtype=torch.bfloat16)
+    ref = oracle_prefill(inp)["out"]
+    assert out.dtype == torch.bfloat16
+    assert_rms_close(out.float(), ref, 2e-3, "bf16 out", extra=half_ulp_bf16(ref))
+
+
+def test_prefill_channel_slice_views():
+    """x/z/dt, params, out and states as channel-slice views of wider tensors (the TP shard layout)."""
+    Dfull, lo, hi = 160, 32, 128
+    inp = make_mixer_inputs(2, 150, Dfull, dtype=torch.bfloat16, seed=9).to(DEV)
+    cs, ss = (t.to(DEV) for t in make_states(2, Dfull, seed=3))
+    sl = slice(lo, hi)
+    out_full = torch.full((2, 150, Dfull), float("nan"), device=DEV)
+    cso_full = torch.full((2, 3, Dfull), float("nan"), device=DEV)
+    sso_full = torch.full((2, Dfull, 16), float("nan"), device=DEV)
+    ssm.prefill(inp.x[..., sl], inp.z[..., sl], inp.dt[..., sl], inp.B, inp.C, inp.A[sl].contiguous(),
+                inp.D[sl].contiguous(), inp.dt_bias[sl].contiguous(), inp.conv_w[sl].contiguous(),
+                inp.conv_b[sl].contiguous(), conv_state_in=cs[:, :, sl], ssm_state_in=ss[:, sl],
+                out=out_full[..., sl], conv_state_out=cso_full[:, :, sl], ssm_state_out=sso_full[:, sl])
+    torch.cuda.synchronize()
+    # untouched outside the slice
+    assert torch.isnan(out_full[..., :lo]).all() and torch.isnan(out_full[..., hi:]).all()
+    assert torch.isnan(sso_full[:, :lo]).all() and torch.isnan(cso_full[:, :, hi:]).all()
+    idx = np.arange(lo, hi)
+    ref = oracle_prefill(cpu_channels(inp, idx), cs[:, :, sl].cpu(), ss[:, sl].cpu())
+    assert_rms_close(out_full[..., sl], ref["out"], 2e-3, "slice out")
+    assert_rms_close(sso_full[:, sl], ref["ssm_state"], 2e-3, "slice state")
+    assert np.array_equal(cso_full[:, :, sl].cpu().double().numpy(), ref["conv_state"])
+
+
+def test_split_invariance_bit_exact_small():
+    """Each channel's result is bit-identical whether it runs in the full call or in a slice."""
+    D = 256
+    inp = make_mixer_inputs(2, 333, D, dtype=torch.bfloat16, seed=13).to(DEV)
+    full, cfull, sfull = run_prefill(inp)
+    for lo, hi in ((0, 64), (64, 128), (128, 200), (200, 256)):
+        sl = slice(lo, hi)
+        o, c, s = ssm.prefill(inp.x[..., sl], inp.z[..., sl], inp.dt[..., sl], inp.B, inp.C,
+                              inp.A[sl].contiguous(), inp.D[sl].contiguous(), inp.dt_bias[sl].contiguous(),
+                              inp.conv_w[sl].contiguous(), inp.conv_b[sl].contiguous())
+        assert torch.equal(o, full[..., sl]), (lo, hi)
+        assert torch.equal(s, sfull[:, sl]), (lo, hi)
+        assert torch.equal(c, cfull[:, :, sl]), (lo, hi)
+
+
+def test_prefill_resumes_from_cached_state():
+    """Chunked prefill: prefill(L1) then prefill(L2) from its states equals prefill(L1 + L2)."""
+    inp = make_mixer_inputs(2, 400, 64, dtype=torch.float32, seed=17)
+    g = inp.to(DEV)
+    full, _, sfull = run_prefill(g)
+    a, ca, sa = run_prefill(inp.token_slice(0, 150).to(DEV))
+    b, cb, sb = run_prefill(inp.token_slice(150, 400).to(DEV), ca, sa)
+    ref = oracle_prefill(inp)
+    assert_rms_close(torch.cat([a, b], 1), ref["out"], 1e-5, "resumed out")
+    assert_rms_close(sb, ref["ssm_state"], 1e-5, "resumed state")
+    assert_rms_close(torch.cat([a, b], 1), full.cpu().double().numpy(), 1e-5, "resumed vs one call")
+
+
+def test_prefill_stream_argument():
+    """The call is enqueued on the stream it is given."""
+    inp = make_mixer_inputs(1, 100, 32, dtype=torch.bfloat16, seed=19).to(DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out, _, _ = run_prefill(inp)
+    s.synchronize()
+    ref = oracle_prefill(inp.to("cpu"))
+    assert_rms_close(out, ref["out"], 2e-3, "stream out")
