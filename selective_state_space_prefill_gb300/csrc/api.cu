@@ -11,7 +11,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/ssm.h"
+#include "ssm.h"
 #include "kernels.h"
 
 namespace {

@@ -36,11 +36,30 @@ __device__ __forceinline__ float silu(float x) {
     return __fdividef(x, 1.0f + ex2(-x * kLog2e));
 }
 
-// softplus(v) = log(1 + e^v).  Above 20 the correction log1p(e^-v) < 2.1e-9 is
-// below fp32 resolution of v, so v is returned.  Below it log1pf keeps full
-// relative accuracy when e^v is tiny (where log(1 + e^v) would cancel).
+// log2(x) with the MUFU.LG2 unit (lg2.approx.ftz.f32).
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// softplus(v) = log(1 + e^v), with e = e^v from MUFU.EX2:
+//   v > 20       -> v: the correction log1p(e^-v) < 2.1e-9 is below the fp32 resolution of v;
+//   e < 1/16     -> log1p(e) by its alternating Taylor series e - e^2/2 + e^3/3 - e^4/4 + e^5/5
+//                   (Horner form); the first dropped term bounds the relative error by
+//                   e^5/6 < 1.6e-7, and there is no cancellation however small e is;
+//   otherwise    -> log2(1 + e) * ln 2 through MUFU.LG2; 1 + e carries at most 2^-24 absolute
+//                   rounding and the result is at least log(17/16) = 0.06, so the relative
+//                   error stays near 1e-6.
 __device__ __forceinline__ float softplus(float v) {
-    return v > 20.0f ? v : log1pf(ex2(v * kLog2e));
+    const float e = ex2(v * kLog2e);
+    float s = fmaf(e, 0.2f, -0.25f);
+    s = fmaf(e, s, 1.0f / 3.0f);
+    s = fmaf(e, s, -0.5f);
+    s = fmaf(e, s, 1.0f);
+    const float series = e * s;
+    const float viaLog = lg2(1.0f + e) * kLn2;
+    return v > 20.0f ? v : (e < 0.0625f ? series : viaLog);
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

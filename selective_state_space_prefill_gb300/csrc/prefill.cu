@@ -9,19 +9,23 @@
 // Methodology 2, local recurrence) and the final states are the cache that
 // decode continues from (Methodology 3).
 //
-// Design (one GB300, HBM- and ALU-bound; no tensor cores: the recurrence is
-// diagonal, not a contraction):
-//   * One CTA owns 32 channels (one per lane) of one batch row for the WHOLE
-//     sequence, so the carry between time chunks stays in registers: no
-//     scratch memory, no inter-CTA waits, one launch.
+// Design (one GB300; the path is bound by the FP32/MUFU pipes and instruction
+// issue, with HBM next; no tensor cores: the recurrence is diagonal, not a
+// contraction):
+//   * One CTA owns 16 channels of one batch row for the WHOLE sequence, so the
+//     carry between time chunks stays in registers: no scratch memory, no
+//     inter-CTA waits, one launch.
+//   * Lane l of a warp works on channel l % 16 and on half g = l / 16 of the 16
+//     states (states 8g .. 8g+7, as four f32x2 pairs).  The two halves of a
+//     channel share the per-token work: each computes conv/SiLU/softplus for half
+//     of the tokens and the results meet through shuffles; their partial
+//     readouts C.h meet the same way.
 //   * Time advances in chunks of TC = S*K tokens.  Warp j of the S warps owns the
-//     K consecutive tokens [j*K, j*K + K) of the chunk; inside a warp every lane
-//     runs the same tokens for its own channel, so B_t/C_t reads are shared-memory
-//     broadcasts and x/z/dt/out accesses are 32 consecutive channels.
+//     K consecutive tokens [j*K, j*K + K) of the chunk.
 //   * Staging: a 3-stage ring of TMA tile copies (x with a 3-token conv halo,
-//     z, dt as [TC x 32] boxes; B, C as [TC x 16] boxes) completing on mbarriers,
-//     issued one chunk ahead by one thread.  Out-of-range rows/channels arrive
-//     as zeros.
+//     z, dt as [TC x 16] boxes; B, C as [TC x 16] boxes) completing on mbarriers,
+//     issued two chunks ahead by one thread.  Out-of-range rows/channels arrive
+//     as zeros.  B and C are widened to fp32 once per chunk by the whole CTA.
 //   * The scan is a chunked associative scan of (a, b) pairs, two states at a
 //     time in packed f32x2 arithmetic:
 //       1. per lane, a_i = 2^(delta_i A'[n]), b_i = delta_i u_i B_i[n] for its K
@@ -45,7 +49,7 @@ namespace ssm {
 
 namespace {
 
-constexpr int kCD = 32;      // channels per CTA (one per lane)
+constexpr int kCD = 16;      // channels per CTA
 constexpr int kN = 16;       // d_state
 constexpr int kStages = 3;   // TMA ring depth
 
@@ -66,10 +70,11 @@ struct Layout {
     static constexpr int OFF_C = align128(OFF_B + BC_BYTES);
     static constexpr int STAGE = align128(OFF_C + BC_BYTES);
     static constexpr int TX = X_BYTES + 2 * Z_BYTES + 2 * BC_BYTES;   // bytes per stage fill
-    // after the ring: fp32 copies of B and C for the chunk, the exchange slots, barriers
-    static constexpr int OFF_BF = kStages * STAGE;
-    static constexpr int OFF_CF = OFF_BF + TC * kN * 4;
-    static constexpr int OFF_XCH = OFF_CF + TC * kN * 4;
+    // after the ring: fp32 B and C of the chunk (two parities), the exchange slots, barriers
+    static constexpr int BCF = TC * kN * 4;
+    static constexpr int OFF_BF = kStages * STAGE;       // [2][TC][16]
+    static constexpr int OFF_CF = OFF_BF + 2 * BCF;      // [2][TC][16]
+    static constexpr int OFF_XCH = OFF_CF + 2 * BCF;     // [2 slots][S][32] float4
     static constexpr int XCH_BYTES = 2 * S * 32 * 16;
     static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
     static constexpr int TOTAL = OFF_BAR + kStages * 8;
@@ -77,24 +82,34 @@ struct Layout {
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// Two consecutive bf16 / fp32 elements widened to float2.
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ float2 load_pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
+
 template <int S, int K, typename Tin, typename Tout>
-__global__ void __launch_bounds__(S * 32, 1)
+__global__ void __launch_bounds__(S * 32, 3)
 k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_B,
           const __grid_constant__ CUtensorMap tm_C, const PrefillArgs p) {
     using Lay = Layout<S, K, Tin>;
     constexpr int TC = Lay::TC;
+    constexpr int KH = K / 2;            // tokens whose per-token work this lane does
+    static_assert(K % 2 == 0, "K must be even");
     extern __shared__ __align__(128) unsigned char smem[];
-    float* Bf = reinterpret_cast<float*>(smem + Lay::OFF_BF);
-    float* Cf = reinterpret_cast<float*>(smem + Lay::OFF_CF);
+    float* Bf0 = reinterpret_cast<float*>(smem + Lay::OFF_BF);
+    float* Cf0 = reinterpret_cast<float*>(smem + Lay::OFF_CF);
     float4* xch = reinterpret_cast<float4*>(smem + Lay::OFF_XCH);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::OFF_BAR);
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int c = lane & 15;             // channel within the CTA
+    const int g = lane >> 4;             // state half: states 8g .. 8g+7
     const int d0 = blockIdx.x * kCD;
     const int b = blockIdx.y;
-    const int d = d0 + lane;
+    const int d = d0 + c;
     const bool dvalid = d < p.d_inner;
     const int L = p.seqlen;
     const int n_iter = (L + TC - 1) / TC;
@@ -131,17 +146,17 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
 
     // ---- per-channel parameters (zeros for channels past d_inner)
-    float A2[kN];   // A * log2(e): exp(delta A) = 2^(delta A2)
+    float A2[8];    // A[d][8g + m] * log2(e): exp(delta A) = 2^(delta A2)
     float Dd = 0.f, bias = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f, cb = 0.f;
-    float2 carry[kN / 2];
+    float2 carry[4];
 #pragma unroll
-    for (int n = 0; n < kN; ++n) A2[n] = 0.f;
+    for (int m = 0; m < 8; ++m) A2[m] = 0.f;
 #pragma unroll
-    for (int q = 0; q < kN / 2; ++q) carry[q] = f2(0.f, 0.f);
+    for (int q = 0; q < 4; ++q) carry[q] = f2(0.f, 0.f);
     if (dvalid) {
-        const float4* Ar = reinterpret_cast<const float4*>(p.A + (int64_t)d * kN);
+        const float4* Ar = reinterpret_cast<const float4*>(p.A + (int64_t)d * kN + 8 * g);
 #pragma unroll
-        for (int q = 0; q < kN / 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const float4 v = __ldg(Ar + q);
             A2[4 * q + 0] = v.x * kLog2e;
             A2[4 * q + 1] = v.y * kLog2e;
@@ -155,15 +170,33 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         bias = __ldg(p.dt_bias + d);
         if (p.ssm_state_in) {
             const float2* hs = reinterpret_cast<const float2*>(
-                p.ssm_state_in + (int64_t)b * p.ssm_state_stride_b + (int64_t)d * kN);
+                p.ssm_state_in + (int64_t)b * p.ssm_state_stride_b + (int64_t)d * kN + 8 * g);
 #pragma unroll
-            for (int q = 0; q < kN / 2; ++q) carry[q] = hs[q];
+            for (int q = 0; q < 4; ++q) carry[q] = hs[q];
         }
     }
 
     for (int it = 0; it < n_iter; ++it) {
         const int s = it % kStages;
         const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((it / kStages) & 1));
+        const unsigned char* st = smem + s * Lay::STAGE;
+        const Tin* xs = reinterpret_cast<const Tin*>(st + Lay::OFF_X);
+        const Tin* zs = reinterpret_cast<const Tin*>(st + Lay::OFF_Z);
+        const Tin* dts = reinterpret_cast<const Tin*>(st + Lay::OFF_DT);
+        float* Bf = Bf0 + (it & 1) * TC * kN;
+        float* Cf = Cf0 + (it & 1) * TC * kN;
+        if (ok) {
+            // ---- B and C of the chunk widened to fp32 once, by the whole CTA.  The
+            // parity buffer written here was last read in chunk it-2, which every
+            // warp finished before the barriers of chunk it-1.
+            const Tin* Bs = reinterpret_cast<const Tin*>(st + Lay::OFF_B);
+            const Tin* Cs = reinterpret_cast<const Tin*>(st + Lay::OFF_C);
+#pragma unroll
+            for (int e = 2 * threadIdx.x; e < TC * kN; e += 2 * S * 32) {
+                *reinterpret_cast<float2*>(Bf + e) = load_pair(Bs + e);
+                *reinterpret_cast<float2*>(Cf + e) = load_pair(Cs + e);
+            }
+        }
         if (__syncthreads_or(!ok)) {
             // A copy never completed: record it, let every issued copy land (bounded) and stop.
             if (threadIdx.x == 0) {
@@ -174,108 +207,107 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             }
             return;
         }
-        const unsigned char* st = smem + s * Lay::STAGE;
-        const Tin* xs = reinterpret_cast<const Tin*>(st + Lay::OFF_X);
-        const Tin* zs = reinterpret_cast<const Tin*>(st + Lay::OFF_Z);
-        const Tin* dts = reinterpret_cast<const Tin*>(st + Lay::OFF_DT);
-        const Tin* Bs = reinterpret_cast<const Tin*>(st + Lay::OFF_B);
-        const Tin* Cs = reinterpret_cast<const Tin*>(st + Lay::OFF_C);
 
-        // ---- this warp's K rows of B and C, widened to fp32 once
-        {
-            float* bw = Bf + warp * K * kN;
-            float* cw = Cf + warp * K * kN;
-            const Tin* bsrc = Bs + warp * K * kN;
-            const Tin* csrc = Cs + warp * K * kN;
-#pragma unroll
-            for (int e = lane; e < K * kN; e += 32) {
-                bw[e] = to_f32(bsrc[e]);
-                cw[e] = to_f32(csrc[e]);
-            }
-            __syncwarp();
-        }
-
-        // ---- pointwise: conv + SiLU, softplus step, skip term
+        // ---- per-token work for this lane's half of the warp's K tokens:
+        //      conv + SiLU, softplus step, skip term
         const int row0 = warp * K;            // first token of this warp in the chunk
         const int tbase = it * TC + row0;     // its absolute index
-        float xm3 = to_f32(xs[(row0 + 0) * kCD + lane]);   // x[tbase-3]  (tile row 0 = chunk start - 3)
-        float xm2 = to_f32(xs[(row0 + 1) * kCD + lane]);
-        float xm1 = to_f32(xs[(row0 + 2) * kCD + lane]);
-        if (it == 0 && warp == 0 && p.conv_state_in != nullptr && dvalid) {
+        const int r0 = row0 + KH * g;         // first token this lane computes
+        float xm3 = to_f32(xs[(r0 + 0) * kCD + c]);   // x[t-3] (tile row 0 = chunk start - 3)
+        float xm2 = to_f32(xs[(r0 + 1) * kCD + c]);
+        float xm1 = to_f32(xs[(r0 + 2) * kCD + c]);
+        if (it == 0 && warp == 0 && g == 0 && p.conv_state_in != nullptr && dvalid) {
             const float* cs = p.conv_state_in + (int64_t)b * 3 * p.conv_state_ld + d;
             xm3 = cs[0];
             xm2 = cs[p.conv_state_ld];
             xm1 = cs[2 * p.conv_state_ld];
         }
-        float dl[K], du[K], y[K];
+        float dl_own[KH], du_own[KH], ud[KH];
         float dsum = 0.f;
 #pragma unroll
-        for (int i = 0; i < K; ++i) {
-            const float xt = to_f32(xs[(row0 + i + 3) * kCD + lane]);
+        for (int k = 0; k < KH; ++k) {
+            const float xt = to_f32(xs[(r0 + k + 3) * kCD + c]);
             float xc = fmaf(w0, xm3, cb);
             xc = fmaf(w1, xm2, xc);
             xc = fmaf(w2, xm1, xc);
             xc = fmaf(w3, xt, xc);
             xm3 = xm2; xm2 = xm1; xm1 = xt;
             const float u = silu(xc);
-            float delta = softplus(to_f32(dts[(row0 + i) * kCD + lane]) + bias);
-            if (tbase + i >= L) delta = 0.f;   // padding rows: a = 1, b = 0 (identity)
-            dl[i] = delta;
-            du[i] = delta * u;
-            y[i] = Dd * u;
+            float delta = softplus(to_f32(dts[(r0 + k) * kCD + c]) + bias);
+            if (tbase + KH * g + k >= L) delta = 0.f;   // padding rows: a = 1, b = 0 (identity)
+            dl_own[k] = delta;
+            du_own[k] = delta * u;
+            ud[k] = Dd * u;
             dsum += delta;
         }
-
-        // ---- the scan, two states at a time
-        const float* bw = Bf + warp * K * kN;
-        const float* cw = Cf + warp * K * kN;
+        // the two halves of the channel trade their tokens' delta and delta*u
+        float dl[K], du[K];
 #pragma unroll
-        for (int pr = 0; pr < kN / 2; ++pr) {
-            const float2 Ap = f2(A2[2 * pr], A2[2 * pr + 1]);
+        for (int k = 0; k < KH; ++k) {
+            dl[k] = __shfl_sync(0xffffffffu, dl_own[k], c);
+            dl[KH + k] = __shfl_sync(0xffffffffu, dl_own[k], c + 16);
+            du[k] = __shfl_sync(0xffffffffu, du_own[k], c);
+            du[KH + k] = __shfl_sync(0xffffffffu, du_own[k], c + 16);
+        }
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, 16);
+
+        // ---- the scan, two states at a time (pairs 4g .. 4g+3 of this lane)
+        float ylane[K];
+#pragma unroll
+        for (int i = 0; i < K; ++i) ylane[i] = 0.f;
+        const float* bw = Bf + row0 * kN + 8 * g;
+        const float* cw = Cf + row0 * kN + 8 * g;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float2 Ap = f2(A2[2 * r], A2[2 * r + 1]);
             float2 a[K], bb[K];
             float2 agg = f2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < K; ++i) {
                 const float2 e = __fmul2_rn(f2(dl[i], dl[i]), Ap);
                 a[i] = f2(ex2(e.x), ex2(e.y));
-                const float2 Bi = *reinterpret_cast<const float2*>(bw + i * kN + 2 * pr);
+                const float2 Bi = *reinterpret_cast<const float2*>(bw + i * kN + 2 * r);
                 bb[i] = __fmul2_rn(f2(du[i], du[i]), Bi);
                 agg = __ffma2_rn(a[i], agg, bb[i]);
             }
             const float2 ea = __fmul2_rn(f2(dsum, dsum), Ap);
-            xch[((pr & 1) * S + warp) * 32 + lane] = make_float4(ex2(ea.x), ex2(ea.y), agg.x, agg.y);
+            xch[((r & 1) * S + warp) * 32 + lane] = make_float4(ex2(ea.x), ex2(ea.y), agg.x, agg.y);
             __syncthreads();
-            if (pr == 0 && threadIdx.x == 0 && it + kStages - 1 < n_iter) {
+            if (r == 0 && threadIdx.x == 0 && it + kStages - 1 < n_iter) {
                 // every warp has finished chunk it-1, so its stage can be refilled
                 issue(it + kStages - 1);
             }
-            float2 h = carry[pr], hs = h;
+            float2 h = carry[r], hs = h;
 #pragma unroll
             for (int j = 0; j < S; ++j) {
-                const float4 e = xch[((pr & 1) * S + j) * 32 + lane];
+                const float4 e = xch[((r & 1) * S + j) * 32 + lane];
                 if (j == warp) hs = h;
                 h = __ffma2_rn(f2(e.x, e.y), h, f2(e.z, e.w));
             }
-            carry[pr] = h;
+            carry[r] = h;
             h = hs;
 #pragma unroll
             for (int i = 0; i < K; ++i) {
                 h = __ffma2_rn(a[i], h, bb[i]);
-                const float2 Ci = *reinterpret_cast<const float2*>(cw + i * kN + 2 * pr);
-                y[i] = fmaf(Ci.x, h.x, fmaf(Ci.y, h.y, y[i]));
+                const float2 Ci = *reinterpret_cast<const float2*>(cw + i * kN + 2 * r);
+                ylane[i] = fmaf(Ci.x, h.x, fmaf(Ci.y, h.y, ylane[i]));
             }
         }
 
-        // ---- gate and store
-        if (dvalid) {
-            Tout* o = reinterpret_cast<Tout*>(p.out) + (int64_t)b * p.out_stride_b + d;
+        // ---- the two halves' readouts meet; each lane gates and stores its own tokens
+        const int t_own = tbase + KH * g;
 #pragma unroll
-            for (int i = 0; i < K; ++i) {
-                const int t = tbase + i;
-                if (t < L) {
-                    const float g = silu(to_f32(zs[(row0 + i) * kCD + lane]));
-                    o[(int64_t)t * p.out_stride_t] = from_f32<Tout>(y[i] * g);
-                }
+        for (int k = 0; k < KH; ++k) {
+            const float o0 = __shfl_xor_sync(0xffffffffu, ylane[k], 16);
+            const float o1 = __shfl_xor_sync(0xffffffffu, ylane[KH + k], 16);
+            const float mine = g ? ylane[KH + k] : ylane[k];
+            const float other = g ? o1 : o0;
+            const int t = t_own + k;
+            if (dvalid && t < L) {
+                const float yv = (mine + other) + ud[k];
+                const float gz = silu(to_f32(zs[(r0 + k) * kCD + c]));
+                reinterpret_cast<Tout*>(p.out)[(int64_t)b * p.out_stride_b + (int64_t)t * p.out_stride_t + d] =
+                    from_f32<Tout>(yv * gz);
             }
         }
     }
@@ -283,21 +315,23 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     // ---- final states: h_L and the last three raw inputs
     if (warp == 0 && dvalid) {
         float2* hs = reinterpret_cast<float2*>(p.ssm_state_out + (int64_t)b * p.ssm_state_stride_b +
-                                               (int64_t)d * kN);
+                                               (int64_t)d * kN + 8 * g);
 #pragma unroll
-        for (int q = 0; q < kN / 2; ++q) hs[q] = carry[q];
-        const Tin* xg = reinterpret_cast<const Tin*>(p.x) + (int64_t)b * p.in_stride_b + d;
-        float* co = p.conv_state_out + (int64_t)b * 3 * p.conv_state_ld + d;
+        for (int q = 0; q < 4; ++q) hs[q] = carry[q];
+        if (g == 0) {
+            const Tin* xg = reinterpret_cast<const Tin*>(p.x) + (int64_t)b * p.in_stride_b + d;
+            float* co = p.conv_state_out + (int64_t)b * 3 * p.conv_state_ld + d;
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            const int t = L - 3 + k;
-            float v = 0.f;
-            if (t >= 0) {
-                v = to_f32(xg[(int64_t)t * p.in_stride_t]);
-            } else if (p.conv_state_in != nullptr) {
-                v = p.conv_state_in[(int64_t)b * 3 * p.conv_state_ld + (int64_t)(t + 3) * p.conv_state_ld + d];
+            for (int k = 0; k < 3; ++k) {
+                const int t = L - 3 + k;
+                float v = 0.f;
+                if (t >= 0) {
+                    v = to_f32(xg[(int64_t)t * p.in_stride_t]);
+                } else if (p.conv_state_in != nullptr) {
+                    v = p.conv_state_in[(int64_t)b * 3 * p.conv_state_ld + (int64_t)(t + 3) * p.conv_state_ld + d];
+                }
+                co[(int64_t)k * p.conv_state_ld] = v;
             }
-            co[(int64_t)k * p.conv_state_ld] = v;
         }
     }
 }
@@ -317,15 +351,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 3-D map over [dim2][dim1][dim0] elements with byte strides s1 (dim1) and s2 (dim2).
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t dim0,
-              uint64_t dim1, uint64_t dim2, uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1) {
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t dim0, uint64_t dim1,
+              uint64_t dim2, uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[3] = {dim0, dim1, dim2};
     cuuint64_t strides[2] = {s1, s2};
     cuuint32_t box[3] = {box0, box1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    (void)esize;
     CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -344,11 +377,11 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
     const uint64_t st = (uint64_t)a.in_stride_t * es;
     const uint64_t bc_t = (uint64_t)kN * es, bc_b = (uint64_t)a.seqlen * kN * es;
     CUtensorMap mx, mz, mdt, mB, mC;
-    if (!make_map(&mx, a.x, dt, es, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC + 3) ||
-        !make_map(&mz, q.z, dt, es, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
-        !make_map(&mdt, q.dt, dt, es, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
-        !make_map(&mB, q.Bm, dt, es, kN, a.seqlen, q.batch, bc_t, bc_b, kN, TC) ||
-        !make_map(&mC, q.Cm, dt, es, kN, a.seqlen, q.batch, bc_t, bc_b, kN, TC)) {
+    if (!make_map(&mx, a.x, dt, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC + 3) ||
+        !make_map(&mz, q.z, dt, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
+        !make_map(&mdt, q.dt, dt, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
+        !make_map(&mB, q.Bm, dt, kN, a.seqlen, q.batch, bc_t, bc_b, kN, TC) ||
+        !make_map(&mC, q.Cm, dt, kN, a.seqlen, q.batch, bc_t, bc_b, kN, TC)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
         return -1;
     }
