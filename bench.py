@@ -58,6 +58,22 @@ def q8_bytes(P, n, in_es=2, out_es=2):
     return P * n * in_es + n * out_es + n * 4 + ((n + 127) // 128) * 4
 
 
+def max_over_ranks(seconds: float, device=None) -> float:
+    """The slowest rank's time (all ranks call it; without a process group it is the identity)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, slowest_s: float) -> float:
+    """Units processed by all ranks over the slowest rank's time (weak scaling: replicas)."""
+    return world * units_per_rank / slowest_s
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
@@ -245,11 +261,8 @@ def run_ours(args):
     dev_s = sum(step_ms) / 1e3
     if world > 1:
         dist.barrier()
-        t = torch.tensor([dev_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_s = float(t.item())
-    tokens = world * B * L * args.steps
-    value = tokens / dev_s
+    dev_s = max_over_ranks(dev_s, dev)
+    value = whole_job_rate(B * L * args.steps, world, dev_s)
     ms_per_step = 1e3 * dev_s / args.steps
     status = ssm.device_status(clear=True)
 
@@ -300,12 +313,8 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        es = e0.elapsed_time(e1) / 1e3
-        if world > 1:
-            t = torch.tensor([es], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            es = float(t.item())
-        e2e = {"value": world * B * L * args.steps / es, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        es = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+        e2e = {"value": whole_job_rate(B * L * args.steps, world, es), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
     # ---- decode steps/s (batch 1/8/64/256 x d_inner 8192, CUDA graph of 64 steps) and the q8 reduction
@@ -416,6 +425,39 @@ def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4):
     return res
 
 
+def run_profile_target(which: str):
+    """Launch one kernel 4 times (3 warm-up + 1 to capture) for ncu: the prefill on the bench
+    workload, the decode step at batch 256 x d_inner 8192, or q8 over P=4 bf16 [4096, 1, 4096]."""
+    import torch
+    from selective_state_space_prefill_gb300 import build as ssm_build
+    if not ssm_build.up_to_date():
+        ssm_build.build()
+    from selective_state_space_prefill_gb300 import binding as ssm
+    from selective_state_space_prefill_gb300.inputs import (make_decode_inputs, make_mixer_inputs,
+                                                            make_mixer_params, make_partials, make_states)
+    dev = torch.device("cuda", 0)
+    if which == "prefill":
+        w = WORKLOAD
+        inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=torch.bfloat16, seed=0, device=dev)
+        for _ in range(4):
+            ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w, inp.conv_b)
+    elif which == "decode":
+        D, B = 8192, 256
+        par = {k: v.to(dev) for k, v in make_mixer_params(D, seed=1).items()}
+        tok = {k: v.to(dev) for k, v in make_decode_inputs(B, D, seed=B).items()}
+        cs, ss = (t.to(dev) for t in make_states(B, D, seed=B))
+        out = torch.empty(B, D, device=dev)
+        for _ in range(4):
+            ssm.decode_step(tok["x"], tok["z"], tok["dt"], tok["B"], tok["C"], par["A"], par["D"],
+                            par["dt_bias"], par["conv_w"], par["conv_b"], cs, ss, out=out)
+    else:
+        parts = [q.to(dev) for q in make_partials(4, (4096, 1, 4096), dtype=torch.bfloat16, seed=4096)]
+        for _ in range(4):
+            ssm.q8_reduce(parts)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_target": which, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,8 +468,12 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode", "q8"], default=None,
+                    help="only launch one kernel 4 times (for an ncu capture) and exit")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_target(args.profile)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -117,7 +117,7 @@ int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
  * are read and updated IN PLACE (Methodology 3: decode reuses the prefill state).
  * Equals one more token of ssm_prefill.
  *
- *   batch                        number of requests (>= 1)
+ *   batch                        number of requests, 1..65535
  *   x, z, dt                     [batch][D] rows with row stride in_stride_b (>= D)
  *   Bmat, Cmat                   [batch][16] contiguous
  *   A .. conv_b                  as for ssm_prefill

@@ -155,7 +155,7 @@ int ssm_decode_step(int batch, int d_inner, int d_state, int d_conv,
                     void* out, int64_t out_stride_b,
                     void* cuda_stream) {
     g_err[0] = 0;
-    if (batch < 1 || batch > (1 << 24)) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: batch %lld out of range", (long long)(batch));
+    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: batch %lld not in [1, 65535]", (long long)(batch));
     if (d_inner < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: d_inner %lld < 1", (long long)(d_inner));
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: unknown dtype");
     if (d_state != 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_decode_step: d_state %lld unsupported (16 only)", (long long)(d_state));
