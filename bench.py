@@ -74,6 +74,19 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_s: float) -> float
     return world * units_per_rank / slowest_s
 
 
+# DRAM bytes (read + write) of one k_prefill launch on the bench workload, from the ncu capture
+# summarised in profiles/k_prefill_mamba130m_like_b4_l2048_d1536.md, valid only for the prefill
+# source it was taken on (first 16 hex digits of its sha256); any other source reports null.
+PREFILL_NCU_TRAFFIC = {"bytes": 76209664 + 17416448, "prefill_cu_sha256_16": "cce7d03e3c8af809"}
+
+
+def _prefill_traffic():
+    import hashlib
+    src = ROOT / "selective_state_space_prefill_gb300" / "csrc" / "prefill.cu"
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    return PREFILL_NCU_TRAFFIC["bytes"] if digest == PREFILL_NCU_TRAFFIC["prefill_cu_sha256_16"] else None
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
@@ -278,7 +291,7 @@ def run_ours(args):
     fp32_peak = n_sm * 128 * sm_max * 1e6 / 1e12           # TFLOP/s-equivalent: FP32-pipe lane-ops/s
     fp32_ach = prefill_fp32_ops(B, L, D) / avg_s / 1e12
     roofline = {"bound": "alu", "achieved": fp32_ach, "peak": fp32_peak, "unit": "T fp32-ops/s",
-                "frac": fp32_ach / fp32_peak, "traffic": None,
+                "frac": fp32_ach / fp32_peak, "traffic": _prefill_traffic(), "traffic_unit": "DRAM bytes per launch (ncu)",
                 "kernel": "k_prefill", "peak_source": f"{n_sm} SMs x 128 FP32 lanes x {sm_max:.0f} MHz",
                 "hbm": {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                         "frac": achieved_gbs / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
