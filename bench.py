@@ -300,41 +300,15 @@ def run_ours(args):
     # ---- end to end through the public call with host buffers
     e2e = None
     if not args.no_e2e:
-        host = {k: getattr(inp, k).cpu().pin_memory() for k in ("x", "z", "dt", "B", "C")}
-        dbuf = {k: torch.empty_like(getattr(inp, k)) for k in host}
-        hout = torch.empty(B, L, D, dtype=torch.float32).pin_memory()
-        hcs = torch.empty(B, 3, D).pin_memory()
-        hss = torch.empty(B, D, 16).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = hout.numel() * 4 + hcs.numel() * 4 + hss.numel() * 4
-
-        def e2e_step():
-            for k in host:
-                dbuf[k].copy_(host[k], non_blocking=True)
-            ssm.prefill(dbuf["x"], dbuf["z"], dbuf["dt"], dbuf["B"], dbuf["C"], inp.A, inp.D, inp.dt_bias,
-                        inp.conv_w, inp.conv_b, out=out, conv_state_out=cso, ssm_state_out=sso, stream=stream)
-            hout.copy_(out, non_blocking=True)
-            hcs.copy_(cso, non_blocking=True)
-            hss.copy_(sso, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        es = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
-        e2e = {"value": whole_job_rate(B * L * args.steps, world, es), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+        e2e = bench_e2e(ssm, inp, dev, args.steps, world, B, L, D)
 
     # ---- decode steps/s (batch 1/8/64/256 x d_inner 8192, CUDA graph of 64 steps) and the q8 reduction
     extras = {}
     if not args.no_extras:
         extras["decode"] = bench_decode(ssm, dev, stream, hbm_peak)
         extras["q8"] = bench_q8(ssm, dev, stream, hbm_peak, flush)
+        extras["prefill_other_workloads"] = bench_prefill_other(ssm, dev, stream, hbm_peak, flush)
+        extras["decode_block"] = bench_decode_block(ssm, dev, stream, hbm_peak, flush)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -364,6 +338,124 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def bench_e2e(ssm, inp, dev, steps, world, B, L, D):
+    """The same prefill through the public call with host buffers: every step copies x/z/dt/B/C
+    from pinned host memory and out plus both states back.  Copies of step k+1 and k-1 overlap
+    the prefill of step k (three streams, two device buffer sets)."""
+    import torch
+    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("x", "z", "dt", "B", "C")}
+    dbuf = [{k: torch.empty_like(getattr(inp, k)) for k in host} for _ in range(2)]
+    outs = [torch.empty(B, L, D, device=dev) for _ in range(2)]
+    css = [torch.empty(B, 3, D, device=dev) for _ in range(2)]
+    sss = [torch.empty(B, D, 16, device=dev) for _ in range(2)]
+    hout = [torch.empty(B, L, D).pin_memory() for _ in range(2)]
+    hcs = [torch.empty(B, 3, D).pin_memory() for _ in range(2)]
+    hss = [torch.empty(B, D, 16).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = (hout[0].numel() + hcs[0].numel() + hss[0].numel()) * 4
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    comp_done = [ev(), ev()]
+    out_done = [ev(), ev()]
+    for e in comp_done + out_done:
+        e.record(torch.cuda.current_stream(dev))
+
+    def step(k):
+        j = k % 2
+        s_in.wait_event(comp_done[j])                 # input buffers j free again
+        with torch.cuda.stream(s_in):
+            for name in host:
+                dbuf[j][name].copy_(host[name], non_blocking=True)
+        in_done = ev()
+        in_done.record(s_in)
+        s_cmp.wait_event(in_done)
+        s_cmp.wait_event(out_done[j])                 # output buffers j read back already
+        d = dbuf[j]
+        ssm.prefill(d["x"], d["z"], d["dt"], d["B"], d["C"], inp.A, inp.D, inp.dt_bias, inp.conv_w,
+                    inp.conv_b, out=outs[j], conv_state_out=css[j], ssm_state_out=sss[j], stream=s_cmp)
+        comp_done[j].record(s_cmp)
+        s_out.wait_event(comp_done[j])
+        with torch.cuda.stream(s_out):
+            hout[j].copy_(outs[j], non_blocking=True)
+            hcs[j].copy_(css[j], non_blocking=True)
+            hss[j].copy_(sss[j], non_blocking=True)
+        out_done[j].record(s_out)
+
+    for k in range(3):
+        step(k)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    s_cmp.wait_event(e0)
+    s_out.wait_event(e0)
+    for k in range(steps):
+        step(k)
+    s_out.wait_stream(s_cmp)
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    es = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+    return {"value": whole_job_rate(B * L * steps, world, es), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "note": "pinned host buffers; copies of neighbouring steps overlap the prefill (3 streams)"}
+
+
+def bench_prefill_other(ssm, dev, stream, hbm_peak, flush):
+    """Prefill tokens/s on the long-context and channel-slice workloads (5 timed launches each)."""
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_mixer_inputs
+    res = {}
+    for name, (Bt, L, D) in {"zamba7b_like_L65536_d7168": (1, 65536, 7168),
+                             "falcon_mamba7b_like_slice_L16384_d2048": (1, 16384, 2048)}.items():
+        inp = make_mixer_inputs(Bt, L, D, dtype=torch.bfloat16, seed=0, device=dev)
+        out = torch.empty(Bt, L, D, device=dev)
+        cs, ss = torch.empty(Bt, 3, D, device=dev), torch.empty(Bt, D, 16, device=dev)
+        f = lambda: ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w,
+                                inp.conv_b, out=out, conv_state_out=cs, ssm_state_out=ss, stream=stream)
+        for _ in range(3):
+            f()
+        ts = []
+        for k in range(5):
+            flush.fill_(float(k))
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            f()
+            b_.record(stream)
+            ts.append((a, b_))
+        torch.cuda.synchronize(dev)
+        t = statistics.median(a.elapsed_time(b_) for a, b_ in ts) / 1e3
+        gbs = prefill_bytes(Bt, L, D) / t / 1e9
+        res[name] = {"ms": 1e3 * t, "tokens_per_s": Bt * L / t, "GB_s": gbs, "frac_hbm": gbs / hbm_peak}
+        del inp, out
+        torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode_block(ssm, dev, stream, hbm_peak, flush, batch=64, T=8, D=8192):
+    """ssm_decode_tokens: a T-token block per request (speculative / verification tokens)."""
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_mixer_inputs, make_states
+    inp = make_mixer_inputs(batch, T, D, dtype=torch.bfloat16, seed=T, device=dev)
+    cs, ss = (t.to(dev) for t in make_states(batch, D, seed=T))
+    out = torch.empty(batch, T, D, device=dev)
+    f = lambda: ssm.decode_tokens(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w,
+                                  inp.conv_b, cs, ss, out=out, stream=stream)
+    for _ in range(3):
+        f()
+    ts = []
+    for k in range(10):
+        flush.fill_(float(k))
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        f()
+        b_.record(stream)
+        ts.append((a, b_))
+    torch.cuda.synchronize(dev)
+    t = statistics.median(a.elapsed_time(b_) for a, b_ in ts) / 1e3
+    nbytes = batch * D * (128 + 24) + batch * T * D * (3 * 2 + 4) + D * 92 + batch * T * 64
+    return {"batch": batch, "tokens_per_request": T, "d_inner": D, "us": 1e6 * t,
+            "tokens_per_s": batch * T / t, "GB_s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak}
 
 
 def bench_decode(ssm, dev, stream, hbm_peak, steps=64, D=8192):

@@ -142,6 +142,35 @@ int ssm_decode_step(int batch, int d_inner, int d_state, int d_conv,
                     void* cuda_stream);
 
 /*
+ * ssm_decode_tokens -- n_tokens >= 1 tokens per request, continuing from the cached
+ * states and updating them in place (Methodology 3): the same result as n_tokens
+ * calls of ssm_decode_step, or as ssm_prefill over those tokens started from the
+ * cached states.  Meant for short blocks (speculative or verification tokens,
+ * 2..16); long prompts belong to ssm_prefill.  ssm_decode_step is n_tokens = 1.
+ *
+ *   batch, n_tokens              1..65535 requests, 1..4096 tokens each
+ *   x, z, dt                     [batch][n_tokens][D] views: element (r, t, d) at
+ *                                r*in_stride_b + t*in_stride_t + d (in_stride_t >= D)
+ *   Bmat, Cmat                   [batch][n_tokens][16] contiguous
+ *   conv_state, ssm_state,
+ *   n_slots, state_slot          as for ssm_decode_step
+ *   out                          [batch][n_tokens][D] view with out_stride_b, out_stride_t;
+ *                                requests may not overlap
+ */
+int ssm_decode_tokens(int batch, int n_tokens, int d_inner, int d_state, int d_conv,
+                      ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                      const void* x, const void* z, const void* dt,
+                      int64_t in_stride_b, int64_t in_stride_t,
+                      const void* Bmat, const void* Cmat,
+                      const float* A, const float* Dskip, const float* dt_bias,
+                      const float* conv_w, const float* conv_b,
+                      float* conv_state, float* ssm_state,
+                      int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                      int n_slots, const int32_t* state_slot,
+                      void* out, int64_t out_stride_b, int64_t out_stride_t,
+                      void* cuda_stream);
+
+/*
  * q8_reduce_partials -- the arithmetic of the pages' 8-bit quantized all-reduce
  * (Methodology 4), done locally over P partial buffers already in this GPU's
  * memory: quantize every partial to int8 with one scale per block of `block`

@@ -20,7 +20,7 @@ _STATUS = {0: "SSM_OK", -1: "SSM_ERR_INVALID_ARG", -2: "SSM_ERR_UNSUPPORTED", -3
            -4: "SSM_ERR_CUDA", -5: "SSM_ERR_DEVICE_TIMEOUT"}
 DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
 
-EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_decode_step", "q8_reduce_partials",
+EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_decode_step", "ssm_decode_tokens", "q8_reduce_partials",
            "ssm_device_status", "ssm_last_error")
 
 
@@ -54,6 +54,9 @@ def load(path: Path | str | None = None):
     lib.ssm_decode_step.argtypes = [I, I, I, I, I, I, P, P, P, L, P, P, P, P, P, P, P, P, P, L, L, I, P,
                                     P, L, P]
     lib.ssm_decode_step.restype = I
+    lib.ssm_decode_tokens.argtypes = [I, I, I, I, I, I, I, P, P, P, L, L, P, P, P, P, P, P, P, P, P, L, L, I,
+                                      P, P, L, L, P]
+    lib.ssm_decode_tokens.restype = I
     lib.q8_reduce_partials.argtypes = [I, P, I, L, I, P, I, P, P, P]
     lib.q8_reduce_partials.restype = I
     lib.ssm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
@@ -198,6 +201,43 @@ def decode_step(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state, ssm_s
                              _ptr(conv_state), _ptr(ssm_state), ld, sb, n_slots, _ptr(state_slot),
                              _ptr(out), out.stride(0), _stream(stream))
     _check(lib, "ssm_decode_step", rc)
+    return out
+
+
+def decode_tokens(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state, ssm_state, state_slot=None,
+                  out=None, out_dtype=torch.float32, stream=None):
+    """ssm_decode_tokens: x/z/dt [batch, T, d_inner] (channel-stride-1 views), B/C [batch, T, 16];
+    the cached states (as for decode_step) advance T tokens in place.  Returns out [batch, T, d_inner]."""
+    lib = load()
+    _need_cuda(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state, ssm_state, state_slot)
+    batch, T, d_inner = x.shape
+    if z.shape != x.shape or dt.shape != x.shape or z.stride() != x.stride() or dt.stride() != x.stride():
+        raise ValueError("x, z, dt must share shape and strides")
+    _chan_contig(x, "x")
+    for t, n in ((B, "B"), (C, "C")):
+        if tuple(t.shape) != (batch, T, 16) or not t.is_contiguous() or t.dtype != x.dtype:
+            raise ValueError(f"{n} must be contiguous [batch, T, 16] of the input dtype")
+    _param(A, (d_inner, 16), "A")
+    for t, n in ((D, "D"), (dt_bias, "dt_bias"), (conv_b, "conv_b")):
+        _param(t, (d_inner,), n)
+    _param(conv_w, (d_inner, 4), "conv_w")
+    n_slots = conv_state.shape[0]
+    if ssm_state.shape[0] != n_slots:
+        raise ValueError("conv_state and ssm_state must have the same number of slots")
+    ld = _conv_state_layout(conv_state, n_slots, d_inner, "conv_state")
+    sb = _ssm_state_layout(ssm_state, n_slots, d_inner, "ssm_state")
+    if state_slot is not None and (state_slot.dtype != torch.int32 or tuple(state_slot.shape) != (batch,)
+                                   or not state_slot.is_contiguous()):
+        raise ValueError("state_slot must be contiguous int32 [batch]")
+    if out is None:
+        out = torch.empty(batch, T, d_inner, device=x.device, dtype=out_dtype)
+    _chan_contig(out, "out")
+    rc = lib.ssm_decode_tokens(batch, T, d_inner, 16, 4, _dtype_code(x.dtype), _dtype_code(out.dtype),
+                               _ptr(x), _ptr(z), _ptr(dt), x.stride(0), x.stride(1), _ptr(B), _ptr(C),
+                               _ptr(A), _ptr(D), _ptr(dt_bias), _ptr(conv_w), _ptr(conv_b),
+                               _ptr(conv_state), _ptr(ssm_state), ld, sb, n_slots, _ptr(state_slot),
+                               _ptr(out), out.stride(0), out.stride(1), _stream(stream))
+    _check(lib, "ssm_decode_tokens", rc)
     return out
 
 

@@ -143,55 +143,67 @@ int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
     return SSM_OK;
 }
 
-int ssm_decode_step(int batch, int d_inner, int d_state, int d_conv,
-                    ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
-                    const void* x, const void* z, const void* dt, int64_t in_stride_b,
-                    const void* Bmat, const void* Cmat,
-                    const float* A, const float* Dskip, const float* dt_bias,
-                    const float* conv_w, const float* conv_b,
-                    float* conv_state, float* ssm_state,
-                    int64_t conv_state_ld, int64_t ssm_state_stride_b,
-                    int n_slots, const int32_t* state_slot,
-                    void* out, int64_t out_stride_b,
-                    void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by ssm_decode_step (one token) and ssm_decode_tokens (T tokens).
+int decode_impl(const char* fn, int batch, int n_tokens, int d_inner, int d_state, int d_conv,
+                ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                const void* x, const void* z, const void* dt, int64_t in_stride_b, int64_t in_stride_t,
+                const void* Bmat, const void* Cmat,
+                const float* A, const float* Dskip, const float* dt_bias,
+                const float* conv_w, const float* conv_b,
+                float* conv_state, float* ssm_state,
+                int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                int n_slots, const int32_t* state_slot,
+                void* out, int64_t out_stride_b, int64_t out_stride_t,
+                void* cuda_stream) {
     g_err[0] = 0;
-    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: batch %lld not in [1, 65535]", (long long)(batch));
-    if (d_inner < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: d_inner %lld < 1", (long long)(d_inner));
-    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: unknown dtype");
-    if (d_state != 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_decode_step: d_state %lld unsupported (16 only)", (long long)(d_state));
-    if (d_conv != 4) return fail(SSM_ERR_UNSUPPORTED, "ssm_decode_step: d_conv %lld unsupported (4 only)", (long long)(d_conv));
-    if (d_inner % 8 != 0) return fail(SSM_ERR_UNSUPPORTED, "ssm_decode_step: d_inner %lld is not a multiple of 8", (long long)(d_inner));
+    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: batch %lld not in [1, 65535]", fn, (long long)batch);
+    if (n_tokens < 1 || n_tokens > 4096) return fail(SSM_ERR_INVALID_ARG, "%s: n_tokens %lld not in [1, 4096]", fn, (long long)n_tokens);
+    if (d_inner < 1) return fail(SSM_ERR_INVALID_ARG, "%s: d_inner %lld < 1", fn, (long long)d_inner);
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (d_state != 16) return fail(SSM_ERR_UNSUPPORTED, "%s: d_state %lld unsupported (16 only)", fn, (long long)d_state);
+    if (d_conv != 4) return fail(SSM_ERR_UNSUPPORTED, "%s: d_conv %lld unsupported (4 only)", fn, (long long)d_conv);
+    if (d_inner % 8 != 0) return fail(SSM_ERR_UNSUPPORTED, "%s: d_inner %lld is not a multiple of 8", fn, (long long)d_inner);
     if (!x || !z || !dt || !Bmat || !Cmat || !A || !Dskip || !dt_bias || !conv_w || !conv_b || !conv_state ||
         !ssm_state || !out)
-        return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: a required pointer is NULL");
-    if (in_stride_b < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: in_stride_b %lld < d_inner", (long long)(in_stride_b));
-    if (out_stride_b < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: out_stride_b %lld < d_inner", (long long)(out_stride_b));
-    if (conv_state_ld < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: conv_state_ld %lld < d_inner", (long long)(conv_state_ld));
+        return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (n_tokens > 1 && in_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "%s: in_stride_t %lld < d_inner", fn, (long long)in_stride_t);
+    if (n_tokens > 1 && out_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "%s: out_stride_t %lld < d_inner", fn, (long long)out_stride_t);
+    const int64_t in_row = n_tokens > 1 ? (int64_t)(n_tokens - 1) * in_stride_t + d_inner : d_inner;
+    const int64_t out_row = n_tokens > 1 ? (int64_t)(n_tokens - 1) * out_stride_t + d_inner : d_inner;
+    if (batch > 1 && in_stride_b < in_row) return fail(SSM_ERR_INVALID_ARG, "%s: in_stride_b %lld too small", fn, (long long)in_stride_b);
+    if (batch > 1 && out_stride_b < out_row) return fail(SSM_ERR_INVALID_ARG, "%s: out_stride_b %lld lets requests overlap", fn, (long long)out_stride_b);
+    if (conv_state_ld < d_inner) return fail(SSM_ERR_INVALID_ARG, "%s: conv_state_ld %lld < d_inner", fn, (long long)conv_state_ld);
     if (ssm_state_stride_b < 16LL * d_inner)
-        return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: ssm_state_stride_b %lld < 16*d_inner", (long long)(ssm_state_stride_b));
+        return fail(SSM_ERR_INVALID_ARG, "%s: ssm_state_stride_b %lld < 16*d_inner", fn, (long long)ssm_state_stride_b);
     if (n_slots < 1 || (!state_slot && n_slots < batch))
-        return fail(SSM_ERR_INVALID_ARG, "ssm_decode_step: n_slots %lld too small", (long long)(n_slots));
+        return fail(SSM_ERR_INVALID_ARG, "%s: n_slots %lld too small", fn, (long long)n_slots);
     const int es = esize(in_dtype);
     if (!aligned(Bmat, 4 * es) || !aligned(Cmat, 4 * es))
-        return fail(SSM_ERR_MISALIGNED, "ssm_decode_step: B and C must be aligned to 4 elements");
+        return fail(SSM_ERR_MISALIGNED, "%s: B and C must be aligned to 4 elements", fn);
     if (!aligned(A, 16) || !aligned(conv_w, 16) || !aligned(ssm_state, 16) || ssm_state_stride_b % 4 != 0)
-        return fail(SSM_ERR_MISALIGNED, "ssm_decode_step: A, conv_w and ssm_state need 16-byte alignment");
+        return fail(SSM_ERR_MISALIGNED, "%s: A, conv_w and ssm_state need 16-byte alignment", fn);
     if (!aligned(x, es) || !aligned(z, es) || !aligned(dt, es) || !aligned(out, esize(out_dtype)) ||
         !aligned(conv_state, 4) || (state_slot && !aligned(state_slot, 4)))
-        return fail(SSM_ERR_MISALIGNED, "ssm_decode_step: a pointer is not element aligned");
+        return fail(SSM_ERR_MISALIGNED, "%s: a pointer is not element aligned", fn);
 
     int serr = 0;
     unsigned int* status = status_ptr(&serr);
-    if (serr) return fail(SSM_ERR_CUDA, "ssm_decode_step: no usable CUDA device");
+    if (serr) return fail(SSM_ERR_CUDA, "%s: no usable CUDA device", fn);
 
     ssm::DecodeArgs a{};
     a.batch = batch;
+    a.n_tokens = n_tokens;
     a.d_inner = d_inner;
     a.n_slots = n_slots;
     a.x = x;
     a.z = z;
     a.dt = dt;
     a.in_stride_b = in_stride_b;
+    a.in_stride_t = in_stride_t;
     a.Bm = Bmat;
     a.Cm = Cmat;
     a.A = A;
@@ -206,12 +218,52 @@ int ssm_decode_step(int batch, int d_inner, int d_state, int d_conv,
     a.state_slot = state_slot;
     a.out = out;
     a.out_stride_b = out_stride_b;
+    a.out_stride_t = out_stride_t;
     a.status = status;
     const char* why = "";
     if (ssm::launch_decode(a, in_dtype == SSM_BF16, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream),
                            &why) != 0)
-        return fail(SSM_ERR_CUDA, "ssm_decode_step: %s", why);
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
     return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_decode_step(int batch, int d_inner, int d_state, int d_conv,
+                    ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                    const void* x, const void* z, const void* dt, int64_t in_stride_b,
+                    const void* Bmat, const void* Cmat,
+                    const float* A, const float* Dskip, const float* dt_bias,
+                    const float* conv_w, const float* conv_b,
+                    float* conv_state, float* ssm_state,
+                    int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                    int n_slots, const int32_t* state_slot,
+                    void* out, int64_t out_stride_b,
+                    void* cuda_stream) {
+    return decode_impl("ssm_decode_step", batch, 1, d_inner, d_state, d_conv, in_dtype, out_dtype, x, z, dt,
+                       in_stride_b, d_inner, Bmat, Cmat, A, Dskip, dt_bias, conv_w, conv_b, conv_state, ssm_state,
+                       conv_state_ld, ssm_state_stride_b, n_slots, state_slot, out, out_stride_b, d_inner,
+                       cuda_stream);
+}
+
+int ssm_decode_tokens(int batch, int n_tokens, int d_inner, int d_state, int d_conv,
+                      ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                      const void* x, const void* z, const void* dt,
+                      int64_t in_stride_b, int64_t in_stride_t,
+                      const void* Bmat, const void* Cmat,
+                      const float* A, const float* Dskip, const float* dt_bias,
+                      const float* conv_w, const float* conv_b,
+                      float* conv_state, float* ssm_state,
+                      int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                      int n_slots, const int32_t* state_slot,
+                      void* out, int64_t out_stride_b, int64_t out_stride_t,
+                      void* cuda_stream) {
+    return decode_impl("ssm_decode_tokens", batch, n_tokens, d_inner, d_state, d_conv, in_dtype, out_dtype, x, z,
+                       dt, in_stride_b, in_stride_t, Bmat, Cmat, A, Dskip, dt_bias, conv_w, conv_b, conv_state,
+                       ssm_state, conv_state_ld, ssm_state_stride_b, n_slots, state_slot, out, out_stride_b,
+                       out_stride_t, cuda_stream);
 }
 
 int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype, int64_t n, int block,

@@ -1,4 +1,4 @@
-// decode.cu -- one-token selective-SSM decode step on sm_103a, in place on the
+// decode.cu -- selective-SSM decode on sm_103a: T >= 1 tokens per request, in place on the
 // cached states ("Scaling State-Space Models on Multiple GPUs with Tensor
 // Parallelism", Methodology 3: the state cached at prefill is reused token by
 // token without recomputing the prompt).
@@ -8,6 +8,8 @@
 //   u = SiLU(xc), delta = softplus(dt + dt_bias)
 //   h[n] = exp(delta A[n]) h[n] + delta B[n] u,  y = sum_n C[n] h[n] + D u
 //   out = y SiLU(z);  cs[s] <- (cs[s][1], cs[s][2], x)
+// for each of the request's T tokens in order (T = 1 is the classic decode step;
+// T = 2..16 serves speculative / verification blocks).
 //
 // The step moves ~164 bytes per (request, channel) and needs ~110 instructions
 // on them, so it is bound by HBM (and by launch latency at small batch).  One
@@ -48,52 +50,65 @@ k_decode(const DecodeArgs p) {
         atomicOr(p.status, 2u);
         return;
     }
-    const int64_t ro = (int64_t)r * p.in_stride_b + d;
-    const float xt = to_f32(reinterpret_cast<const Tin*>(p.x)[ro]);
-    const float zt = to_f32(reinterpret_cast<const Tin*>(p.z)[ro]);
-    const float dtt = to_f32(reinterpret_cast<const Tin*>(p.dt)[ro]);
     float* cs = p.conv_state + (int64_t)slot * 3 * p.conv_state_ld + d;
-    const float c0 = cs[0], c1 = cs[p.conv_state_ld], c2 = cs[2 * p.conv_state_ld];
+    float c0 = cs[0], c1 = cs[p.conv_state_ld], c2 = cs[2 * p.conv_state_ld];
     float4* hp = reinterpret_cast<float4*>(p.ssm_state + (int64_t)slot * p.ssm_state_stride_b + (int64_t)d * 16);
     float4 h[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) h[q] = hp[q];
-    const Tin* Bm = reinterpret_cast<const Tin*>(p.Bm) + (int64_t)r * 16;
-    const Tin* Cm = reinterpret_cast<const Tin*>(p.Cm) + (int64_t)r * 16;
+    float4 A2[4];
     const float4* Ar = reinterpret_cast<const float4*>(p.A + (int64_t)d * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 a = Ar[q];
+        A2[q] = make_float4(a.x * kLog2e, a.y * kLog2e, a.z * kLog2e, a.w * kLog2e);
+    }
     const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)d * 4);
     const float cb = p.conv_b[d], Dd = p.Dskip[d], bias = p.dt_bias[d];
 
-    float xc = fmaf(w.x, c0, cb);
-    xc = fmaf(w.y, c1, xc);
-    xc = fmaf(w.z, c2, xc);
-    xc = fmaf(w.w, xt, xc);
-    const float u = silu(xc);
-    const float delta = softplus(dtt + bias);
-    const float du = delta * u;
-    const float dl2 = delta * kLog2e;   // exp(delta A) = 2^(delta log2(e) A)
-    float y = 0.f;
+    for (int t = 0; t < p.n_tokens; ++t) {
+        const int64_t ro = (int64_t)r * p.in_stride_b + (int64_t)t * p.in_stride_t + d;
+        const float xt = to_f32(reinterpret_cast<const Tin*>(p.x)[ro]);
+        const float zt = to_f32(reinterpret_cast<const Tin*>(p.z)[ro]);
+        const float dtt = to_f32(reinterpret_cast<const Tin*>(p.dt)[ro]);
+        const Tin* Bm = reinterpret_cast<const Tin*>(p.Bm) + ((int64_t)r * p.n_tokens + t) * 16;
+        const Tin* Cm = reinterpret_cast<const Tin*>(p.Cm) + ((int64_t)r * p.n_tokens + t) * 16;
+
+        float xc = fmaf(w.x, c0, cb);
+        xc = fmaf(w.y, c1, xc);
+        xc = fmaf(w.z, c2, xc);
+        xc = fmaf(w.w, xt, xc);
+        c0 = c1;
+        c1 = c2;
+        c2 = xt;
+        const float u = silu(xc);
+        const float delta = softplus(dtt + bias);
+        const float du = delta * u;
+        float y = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 Aq = Ar[q];
-        const float4 Bq = Vec4<Tin>::load(Bm + 4 * q);
-        const float4 Cq = Vec4<Tin>::load(Cm + 4 * q);
-        float4 hv = h[q];
-        hv.x = fmaf(ex2(dl2 * Aq.x), hv.x, du * Bq.x);
-        hv.y = fmaf(ex2(dl2 * Aq.y), hv.y, du * Bq.y);
-        hv.z = fmaf(ex2(dl2 * Aq.z), hv.z, du * Bq.z);
-        hv.w = fmaf(ex2(dl2 * Aq.w), hv.w, du * Bq.w);
-        hp[q] = hv;
-        y = fmaf(Cq.x, hv.x, y);
-        y = fmaf(Cq.y, hv.y, y);
-        y = fmaf(Cq.z, hv.z, y);
-        y = fmaf(Cq.w, hv.w, y);
+        for (int q = 0; q < 4; ++q) {
+            const float4 Bq = Vec4<Tin>::load(Bm + 4 * q);
+            const float4 Cq = Vec4<Tin>::load(Cm + 4 * q);
+            float4 hv = h[q];
+            hv.x = fmaf(ex2(delta * A2[q].x), hv.x, du * Bq.x);
+            hv.y = fmaf(ex2(delta * A2[q].y), hv.y, du * Bq.y);
+            hv.z = fmaf(ex2(delta * A2[q].z), hv.z, du * Bq.z);
+            hv.w = fmaf(ex2(delta * A2[q].w), hv.w, du * Bq.w);
+            h[q] = hv;
+            y = fmaf(Cq.x, hv.x, y);
+            y = fmaf(Cq.y, hv.y, y);
+            y = fmaf(Cq.z, hv.z, y);
+            y = fmaf(Cq.w, hv.w, y);
+        }
+        y = fmaf(Dd, u, y);
+        reinterpret_cast<Tout*>(p.out)[(int64_t)r * p.out_stride_b + (int64_t)t * p.out_stride_t + d] =
+            from_f32<Tout>(y * silu(zt));
     }
-    y = fmaf(Dd, u, y);
-    reinterpret_cast<Tout*>(p.out)[(int64_t)r * p.out_stride_b + d] = from_f32<Tout>(y * silu(zt));
-    cs[0] = c1;
-    cs[p.conv_state_ld] = c2;
-    cs[2 * p.conv_state_ld] = xt;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) hp[q] = h[q];
+    cs[0] = c0;
+    cs[p.conv_state_ld] = c1;
+    cs[2 * p.conv_state_ld] = c2;
 }
 
 }  // namespace

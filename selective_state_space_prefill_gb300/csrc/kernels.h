@@ -29,16 +29,16 @@ struct PrefillLaunch {
 };
 
 struct DecodeArgs {
-    int batch, d_inner, n_slots;
+    int batch, n_tokens, d_inner, n_slots;
     const void *x, *z, *dt;
-    int64_t in_stride_b;
+    int64_t in_stride_b, in_stride_t;
     const void *Bm, *Cm;
     const float *A, *Dskip, *dt_bias, *conv_w, *conv_b;
     float *conv_state, *ssm_state;
     int64_t conv_state_ld, ssm_state_stride_b;
     const int32_t* state_slot;
     void* out;
-    int64_t out_stride_b;
+    int64_t out_stride_b, out_stride_t;
     unsigned int* status;
 };
 

@@ -108,3 +108,20 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _prefill(lib) == CUDA
+
+
+def _tokens(lib, **kw):
+    a = dict(batch=4, T=3, d_inner=64, d_state=16, d_conv=4, in_dtype=1, out_dtype=0, x=FAKE, z=FAKE, dt=FAKE,
+             sb=3 * 64, st=64, B=FAKE, C=FAKE, A=FAKE, D=FAKE, dt_bias=FAKE, conv_w=FAKE, conv_b=FAKE,
+             cs=FAKE, ss=FAKE, ld=64, ssb=1024, n_slots=4, slot=None, out=FAKE, ob=3 * 64, ot=64, stream=None)
+    a.update(kw)
+    return lib.ssm_decode_tokens(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), INVALID), (dict(T=5000), INVALID), (dict(st=32), INVALID), (dict(ot=32), INVALID),
+    (dict(ob=64), INVALID), (dict(sb=64), INVALID), (dict(d_state=8), UNSUPPORTED), (dict(ss=FAKE + 4), MISALIGNED),
+])
+def test_decode_tokens_rejects_bad_arguments(lib, kw, code):
+    assert _tokens(lib, **kw) == code
+    assert lib.ssm_last_error().decode().startswith("ssm_decode_tokens")

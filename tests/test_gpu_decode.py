@@ -116,3 +116,57 @@ def test_prefill_then_decode_equals_prefill(dtype, tol):
     assert_rms_close(torch.stack(outs, 1), ref["out"][:, L1:], tol, "decode tail")
     assert_rms_close(ss, ref["ssm_state"], tol, "final ssm_state")
     assert np.array_equal(cs.cpu().double().numpy(), ref["conv_state"])
+
+
+# ---------------------------------------------------------------- multi-token blocks
+@pytest.mark.parametrize("T", [1, 2, 5, 16])
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, 2e-3), (torch.float32, 1e-5)])
+def test_decode_tokens_matches_oracle(T, dtype, tol):
+    """T tokens per request from random cached states = the oracle's prefill of those tokens from the states."""
+    batch, D = 3, 96
+    inp = make_mixer_inputs(batch, T, D, dtype=dtype, seed=100 + T)
+    cs, ss = make_states(batch, D, seed=200 + T)
+    ref = oracle_prefill(inp, cs, ss)
+    g = inp.to(DEV)
+    gcs, gss = cs.to(DEV), ss.to(DEV)
+    out = ssm.decode_tokens(g.x, g.z, g.dt, g.B, g.C, g.A, g.D, g.dt_bias, g.conv_w, g.conv_b, gcs, gss)
+    torch.cuda.synchronize()
+    assert out.shape == (batch, T, D)
+    assert_rms_close(out, ref["out"], tol, "block out")
+    assert_rms_close(gss, ref["ssm_state"], tol, "block state")
+    assert np.array_equal(gcs.cpu().double().numpy(), ref["conv_state"])
+
+
+def test_decode_tokens_one_token_equals_decode_step():
+    D = 128
+    par = {k: v.to(DEV) for k, v in make_mixer_params(D, seed=11).items()}
+    tok = {k: v.to(DEV) for k, v in make_decode_inputs(4, D, seed=12).items()}
+    cs, ss = (t.to(DEV) for t in make_states(4, D, seed=13))
+    cs2, ss2 = cs.clone(), ss.clone()
+    o1 = _gpu_step(tok, par, cs, ss)
+    o2 = ssm.decode_tokens(tok["x"][:, None], tok["z"][:, None], tok["dt"][:, None], tok["B"][:, None].contiguous(),
+                           tok["C"][:, None].contiguous(), par["A"], par["D"], par["dt_bias"], par["conv_w"],
+                           par["conv_b"], cs2, ss2)
+    assert torch.equal(o1, o2[:, 0]) and torch.equal(ss, ss2) and torch.equal(cs, cs2)
+
+
+def test_decode_tokens_slots_and_prefill_continuation():
+    """Prefill 40 tokens into slots 3 and 1, then an 8-token block per request through the slots,
+    against the oracle's 48-token prefill."""
+    D, L1, T = 64, 40, 8
+    inp = make_mixer_inputs(2, L1 + T, D, dtype=torch.bfloat16, seed=21)
+    ref = oracle_prefill(inp)
+    g = inp.to(DEV)
+    _, cs, ss = run_prefill(inp.token_slice(0, L1).to(DEV))
+    conv = torch.zeros(5, 3, D, device=DEV)
+    ssm_s = torch.zeros(5, D, 16, device=DEV)
+    slots = torch.tensor([3, 1], dtype=torch.int32, device=DEV)
+    conv[slots.long()] = cs
+    ssm_s[slots.long()] = ss
+    blk = inp.token_slice(L1, L1 + T).to(DEV)
+    out = ssm.decode_tokens(blk.x, blk.z, blk.dt, blk.B, blk.C, g.A, g.D, g.dt_bias, g.conv_w, g.conv_b, conv, ssm_s,
+                            state_slot=slots)
+    torch.cuda.synchronize()
+    assert_rms_close(out, ref["out"][:, L1:], 2e-3, "block after prefill")
+    assert_rms_close(ssm_s[slots.long()], ref["ssm_state"], 2e-3, "slot states")
+    assert torch.equal(conv[0], torch.zeros(3, D, device=DEV)) and torch.equal(ssm_s[2], torch.zeros(D, 16, device=DEV))
