@@ -9,7 +9,6 @@
 #include <string.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "ssm.h"
 #include "kernels.h"

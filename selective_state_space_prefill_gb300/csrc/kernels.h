@@ -58,6 +58,4 @@ int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why
 int launch_decode(const DecodeArgs& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
 int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
 
-int prefill_chunk_tokens();
-
 }  // namespace ssm

@@ -427,6 +427,4 @@ int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why
                       : launch_t<kS, kK, float, float>(q, stream, why);
 }
 
-int prefill_chunk_tokens() { return kS * kK; }
-
 }  // namespace ssm
