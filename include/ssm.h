@@ -184,6 +184,9 @@ int ssm_decode_tokens(int batch, int n_tokens, int d_inner, int d_state, int d_c
  *   when out_dtype is bf16).  The last block may be shorter than `block`.
  * Bit-exact: S and scale equal any IEEE-fp32 evaluation of the same steps, and
  * |out - sum_p x_p| <= P*scale/2 plus fp32 rounding.
+ * Non-finite partials lie outside the method; they are handled as follows: a NaN
+ * element is ignored by the block maximum and gets code 0; a block holding an
+ * infinity gets scale +inf, codes 0 and NaN outputs.  Other blocks are unaffected.
  *
  *   P                            1..8
  *   partials                     HOST array of P device pointers, each to n elements of

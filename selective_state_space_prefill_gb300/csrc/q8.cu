@@ -6,15 +6,28 @@
 // Per block of 128 elements, one scale shared by the P partials:
 //   amax = max |x_p[i]|;  inv = 127/amax;  scale = amax/127     (IEEE fp32 division)
 //   q_p[i] = rne(x_p[i] * inv) in [-127, 127];  S[i] = sum_p q_p[i];  out[i] = S[i] * scale
-// Every fp32 step is a correctly rounded operation (__fdiv_rn, __fmul_rn,
-// __float2int_rn, __int2float_rn), so S and scale are bit-identical to any
-// IEEE-fp32 evaluation of the same steps.
+// Every fp32 step is a correctly rounded operation, so S and scale are
+// bit-identical to any IEEE-fp32 evaluation of the same steps.
 //
 // Layout: 16 lanes per 128-element block, each lane owning 8 consecutive
 // elements of every partial (one 16-byte load per bf16 partial, two per fp32
-// partial), so a warp covers two blocks and keeps P x 16 bytes per lane in
-// flight; the block maximum is a 4-step shuffle reduction inside the half-warp.
-// Pure streaming: read P*2 bytes, write 2-4 (+4 for the sums) bytes per element.
+// partial), so a warp covers two blocks.  The partials stay in registers as the
+// raw 32-bit words they were loaded as (two bf16 per word), which keeps the
+// register count low enough for 6 CTAs of 256 threads per SM and so more bytes
+// in flight: the kernel is bound by HBM latency x bytes in flight.
+//
+// Rounding: for a block of finite values, fl(x * inv) lies within 127.5 in
+// magnitude (|x| <= amax, so x * inv <= 127 (1 + 2^-24)), and adding 1.5 * 2^23
+// to it in fp32 rounds it to an integer, ties to even, in the low mantissa bits
+// of the sum; the bits of the P sums are added as integers.  The clamp to
+// [-127, 127] is therefore never active for finite blocks.  The multiply and the
+// add are the scalar __fmul_rn / __fadd_rn, which are never contracted into a
+// fused multiply-add (that would round the unrounded product and break ties).
+// A block holding an Inf or NaN (detected by a NaN-propagating maximum) takes
+// the plain path: NaN-ignoring maximum, round-to-nearest-even conversion and
+// clamp.
+#include <cfloat>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,42 +35,67 @@ namespace ssm {
 namespace {
 
 constexpr int kBlock = 128;
-constexpr int kVec = 8;                     // elements per lane
+constexpr int kVec = 8;                         // elements per lane
 constexpr int kLanesPerBlock = kBlock / kVec;   // 16
-constexpr int kThreads = 256;               // 16 blocks of 128 elements per CTA
+constexpr int kThreads = 256;                   // 16 blocks of 128 elements per CTA
+constexpr uint32_t kMagicBits = 0x4B400000u;    // bits of 1.5 * 2^23
+constexpr float kMagic = 12582912.0f;           // 1.5 * 2^23
 
-__device__ __forceinline__ void load8(const float* p, int64_t i, int64_t n, float v[kVec]) {
-    if (i + kVec - 1 < n) {
-        const float4 a = *reinterpret_cast<const float4*>(p + i);
-        const float4 b = *reinterpret_cast<const float4*>(p + i + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) v[e] = i + e < n ? p[i + e] : 0.f;
-    }
+// |a| and the NaN-propagating maximum of two bf16 pairs, exact.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m, uint32_t w) {
+    uint32_t a, r;
+    asm("abs.bf16x2 %0, %1;" : "=r"(a) : "r"(w));
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(a));
+    return r;
 }
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, int64_t i, int64_t n, float v[kVec]) {
-    if (i + kVec - 1 < n) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(p + i);
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+// kVec elements starting at i as raw 32-bit words; elements at or past n read as 0.
+template <typename Tin>
+__device__ __forceinline__ void load_words(const Tin* p, int64_t i, int64_t n, uint32_t* w) {
+    constexpr int NW = kVec * (int)sizeof(Tin) / 4;
+    if (i + kVec <= n) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-            v[2 * k] = f.x;
-            v[2 * k + 1] = f.y;
+        for (int k = 0; k < NW / 4; ++k) {
+            const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p + i) + k);
+            w[4 * k] = u.x;
+            w[4 * k + 1] = u.y;
+            w[4 * k + 2] = u.z;
+            w[4 * k + 3] = u.w;
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < kVec; ++e) v[e] = i + e < n ? __bfloat162float(p[i + e]) : 0.f;
+        for (int k = 0; k < NW; ++k) {
+            if constexpr (sizeof(Tin) == 2) {
+                const uint16_t* h = reinterpret_cast<const uint16_t*>(p);
+                const uint32_t lo = i + 2 * k < n ? h[i + 2 * k] : 0u;
+                const uint32_t hi = i + 2 * k + 1 < n ? h[i + 2 * k + 1] : 0u;
+                w[k] = lo | (hi << 16);
+            } else {
+                const uint32_t* f = reinterpret_cast<const uint32_t*>(p);
+                w[k] = i + k < n ? f[i + k] : 0u;
+            }
+        }
     }
 }
 
+// Element e of the lane's words, widened to fp32 (exact).
+template <typename Tin>
+__device__ __forceinline__ float elem(const uint32_t* w, int e) {
+    if constexpr (sizeof(Tin) == 2) return (e & 1) ? hi_f32(w[e >> 1]) : lo_f32(w[e >> 1]);
+    else return __uint_as_float(w[e]);
+}
+
 __device__ __forceinline__ void store8(float* p, int64_t i, int64_t n, const float o[kVec]) {
-    if (i + kVec - 1 < n) {
-        *reinterpret_cast<float4*>(p + i) = make_float4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<float4*>(p + i + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    if (i + kVec <= n) {
+        __stcs(reinterpret_cast<float4*>(p + i), make_float4(o[0], o[1], o[2], o[3]));
+        __stcs(reinterpret_cast<float4*>(p + i) + 1, make_float4(o[4], o[5], o[6], o[7]));
     } else {
         for (int e = 0; e < kVec; ++e)
             if (i + e < n) p[i + e] = o[e];
@@ -65,14 +103,14 @@ __device__ __forceinline__ void store8(float* p, int64_t i, int64_t n, const flo
 }
 
 __device__ __forceinline__ void store8(__nv_bfloat16* p, int64_t i, int64_t n, const float o[kVec]) {
-    if (i + kVec - 1 < n) {
+    if (i + kVec <= n) {
         uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * k], o[2 * k + 1]);
             w[k] = *reinterpret_cast<uint32_t*>(&h);
         }
-        *reinterpret_cast<uint4*>(p + i) = make_uint4(w[0], w[1], w[2], w[3]);
+        __stcs(reinterpret_cast<uint4*>(p + i), make_uint4(w[0], w[1], w[2], w[3]));
     } else {
         for (int e = 0; e < kVec; ++e)
             if (i + e < n) p[i + e] = __float2bfloat16_rn(o[e]);
@@ -82,22 +120,49 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, int64_t i, int64_t n, c
 template <typename Tin, typename Tout, int P>
 __global__ void __launch_bounds__(kThreads)
 k_q8(const Q8Args a) {
+    constexpr int NW = kVec * (int)sizeof(Tin) / 4;     // words per lane per partial
     const int64_t blk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
-    const int sub = threadIdx.x % kLanesPerBlock;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % kLanesPerBlock;
     // Every lane takes part in the shuffles; lanes of a block past n just see zeros.
     const int64_t i0 = blk * kBlock + kVec * sub;
 
-    float v[P][kVec];
-    float amax = 0.f;
+    uint32_t w[P][NW];
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-        load8(reinterpret_cast<const Tin*>(a.partials[p]), i0, a.n, v[p]);
+    for (int p = 0; p < P; ++p) load_words<Tin>(reinterpret_cast<const Tin*>(a.partials[p]), i0, a.n, w[p]);
+
+    // block maximum of |x|, NaN-propagating so that a non-finite value shows
+    float amax;
+    if constexpr (sizeof(Tin) == 2) {
+        uint32_t m = 0;
 #pragma unroll
-        for (int e = 0; e < kVec; ++e) amax = fmaxf(amax, fabsf(v[p][e]));
+        for (int p = 0; p < P; ++p)
+#pragma unroll
+            for (int k = 0; k < NW; ++k) m = absmax_bf16x2(m, w[p][k]);
+        amax = max_nan(lo_f32(m), hi_f32(m));
+    } else {
+        amax = 0.f;
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+#pragma unroll
+            for (int k = 0; k < NW; ++k) amax = max_nan(amax, fabsf(__uint_as_float(w[p][k])));
     }
 #pragma unroll
     for (int off = kLanesPerBlock / 2; off > 0; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        amax = max_nan(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const bool finite = amax <= FLT_MAX;          // the same in every lane of the block
+    if (!finite) {
+        // Inf or NaN in the block: the NaN-ignoring maximum, over this block's lanes only
+        const unsigned gmask = 0xffffu << (lane & ~(kLanesPerBlock - 1));
+        amax = 0.f;
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) amax = fmaxf(amax, fabsf(elem<Tin>(w[p], e)));
+#pragma unroll
+        for (int off = kLanesPerBlock / 2; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, off));
+    }
     if (i0 >= a.n) return;
 
     float inv = 0.f, scale = 0.f;
@@ -106,27 +171,44 @@ k_q8(const Q8Args a) {
         scale = __fdiv_rn(amax, 127.0f);
     }
     int s[kVec];
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) s[e] = 0;
-    if (amax > 0.f) {
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-#pragma unroll
-            for (int e = 0; e < kVec; ++e) {
-                int qv = __float2int_rn(__fmul_rn(v[p][e], inv));
-                qv = qv > 127 ? 127 : (qv < -127 ? -127 : qv);
-                s[e] += qv;
-            }
-        }
-    }
     float o[kVec];
+    if (finite) {
+        // bits(fl(fl(x * inv) + 1.5 * 2^23)) = kMagicBits + q; an all-zero block has inv = 0, q = 0
+        uint32_t acc[kVec];
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) o[e] = __fmul_rn(__int2float_rn(s[e]), scale);
+        for (int e = 0; e < kVec; ++e) acc[e] = 0u;
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+#pragma unroll
+            for (int e = 0; e < kVec; ++e)
+                acc[e] += __float_as_uint(__fadd_rn(__fmul_rn(elem<Tin>(w[p], e), inv), kMagic));
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            const uint32_t bits = acc[e] - (uint32_t)(P - 1) * kMagicBits;   // kMagicBits + S, |S| <= 1016
+            s[e] = (int)(bits - kMagicBits);
+            o[e] = __fmul_rn(__fadd_rn(__uint_as_float(bits), -kMagic), scale);   // float(S) is exact
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) s[e] = 0;
+        if (amax > 0.f) {
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) {
+                    int qv = __float2int_rn(__fmul_rn(elem<Tin>(w[p], e), inv));
+                    qv = qv > 127 ? 127 : (qv < -127 ? -127 : qv);
+                    s[e] += qv;
+                }
+        }
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) o[e] = __fmul_rn(__int2float_rn(s[e]), scale);
+    }
     store8(reinterpret_cast<Tout*>(a.out), i0, a.n, o);
     if (a.sums) {
-        if (i0 + kVec - 1 < a.n) {
-            *reinterpret_cast<int4*>(a.sums + i0) = make_int4(s[0], s[1], s[2], s[3]);
-            *reinterpret_cast<int4*>(a.sums + i0 + 4) = make_int4(s[4], s[5], s[6], s[7]);
+        if (i0 + kVec <= a.n) {
+            __stcs(reinterpret_cast<int4*>(a.sums + i0), make_int4(s[0], s[1], s[2], s[3]));
+            __stcs(reinterpret_cast<int4*>(a.sums + i0) + 1, make_int4(s[4], s[5], s[6], s[7]));
         } else {
             for (int e = 0; e < kVec; ++e)
                 if (i0 + e < a.n) a.sums[i0 + e] = s[e];
@@ -146,7 +228,7 @@ int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream,
         return -1;
     }
     dim3 grid((unsigned)ctas);
-    // one instantiation per partial count, so the value registers match P exactly
+    // one instantiation per partial count, so the word registers match P exactly
     switch (a.P) {
 #define SSM_Q8_CASE(PP)                                                                              \
         case PP:                                                                                   \
