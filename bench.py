@@ -403,32 +403,47 @@ def bench_e2e(ssm, inp, dev, steps, world, B, L, D):
 
 
 def bench_prefill_other(ssm, dev, stream, hbm_peak, flush):
-    """Prefill tokens/s on the long-context and channel-slice workloads (5 timed launches each)."""
+    """Prefill tokens/s on the long-context and channel-slice workloads and on a batch-1
+    Mamba-130M-like layer (5 timed launches each, L2 flushed before each).  Batch-1 rows
+    are also timed with the sequence cut into parallel segments (ssm_prefill_segmented,
+    seg_len from binding.suggest_seg_len) when they leave SMs idle."""
     import torch
     from selective_state_space_prefill_gb300.inputs import make_mixer_inputs
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {}
     for name, (Bt, L, D) in {"zamba7b_like_L65536_d7168": (1, 65536, 7168),
-                             "falcon_mamba7b_like_slice_L16384_d2048": (1, 16384, 2048)}.items():
+                             "falcon_mamba7b_like_slice_L16384_d2048": (1, 16384, 2048),
+                             "mamba130m_like_batch1_L2048_d1536": (1, 2048, 1536)}.items():
         inp = make_mixer_inputs(Bt, L, D, dtype=torch.bfloat16, seed=0, device=dev)
         out = torch.empty(Bt, L, D, device=dev)
         cs, ss = torch.empty(Bt, 3, D, device=dev), torch.empty(Bt, D, 16, device=dev)
-        f = lambda: ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w,
-                                inp.conv_b, out=out, conv_state_out=cs, ssm_state_out=ss, stream=stream)
-        for _ in range(3):
-            f()
-        ts = []
-        for k in range(5):
-            flush.fill_(float(k))
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            f()
-            b_.record(stream)
-            ts.append((a, b_))
-        torch.cuda.synchronize(dev)
-        t = statistics.median(a.elapsed_time(b_) for a, b_ in ts) / 1e3
-        gbs = prefill_bytes(Bt, L, D) / t / 1e9
-        res[name] = {"ms": 1e3 * t, "tokens_per_s": Bt * L / t, "GB_s": gbs, "frac_hbm": gbs / hbm_peak}
-        del inp, out
+        seg = ssm.suggest_seg_len(Bt, L, D, n_sm)
+        ws = None
+        if seg is not None:
+            ws = torch.empty(max(1, ssm.prefill_workspace_bytes(Bt, L, D, seg)), device=dev, dtype=torch.uint8)
+        for seg_len in ([None] + ([seg] if seg is not None else [])):
+            f = lambda: ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w,
+                                    inp.conv_b, out=out, conv_state_out=cs, ssm_state_out=ss, stream=stream,
+                                    seg_len=seg_len, workspace=ws if seg_len else None)
+            for _ in range(3):
+                f()
+            ts = []
+            for k in range(5):
+                flush.fill_(float(k))
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                f()
+                b_.record(stream)
+                ts.append((a, b_))
+            torch.cuda.synchronize(dev)
+            t = statistics.median(a.elapsed_time(b_) for a, b_ in ts) / 1e3
+            gbs = prefill_bytes(Bt, L, D) / t / 1e9
+            key = name if seg_len is None else f"{name}_segmented"
+            res[key] = {"ms": 1e3 * t, "tokens_per_s": Bt * L / t, "GB_s": gbs, "frac_hbm": gbs / hbm_peak}
+            if seg_len is not None:
+                res[key].update({"seg_len": seg_len, "segments": -(-L // seg_len),
+                                 "kernels": "k_prefill_agg + k_prefill_carry + k_prefill"})
+        del inp, out, ws
         torch.cuda.empty_cache()
     return res
 

@@ -44,6 +44,7 @@
 #ifndef SSM_H_
 #define SSM_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -111,6 +112,54 @@ int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
                 void* out, int64_t out_stride_b, int64_t out_stride_t,
                 float* conv_state_out, float* ssm_state_out,
                 void* cuda_stream);
+
+/*
+ * ssm_prefill_workspace_bytes -- bytes of device workspace that ssm_prefill_segmented
+ * needs for these sizes: (ceil(seqlen / seg_len) - 1) * batch * d_inner * 128.  Zero when
+ * the row is a single segment or an argument is not positive.
+ */
+size_t ssm_prefill_workspace_bytes(int batch, int seqlen, int d_inner, int seg_len);
+
+/*
+ * ssm_prefill_segmented -- ssm_prefill with every row cut into segments of seg_len
+ * tokens that run in parallel.  The recurrence h_t = a_t h_{t-1} + b_t stays inside
+ * its channel (Methodology 2) and composes associatively, so a segment is summed up
+ * by the pair (product of its a_t, state reached from zero).  A carry pass over the
+ * segments turns the pairs into every segment's start state.  That is the chunked
+ * scan's carry across chunks, taken across thread blocks, and it hands each segment
+ * the state that Methodology 3 caches at the end of the row.
+ * Use it when there are too few rows to fill the GPU: batch * ceil(d_inner / 16)
+ * well below three times the SM count, e.g. batch-1 long-context prefill.  It costs
+ * about 1.4 times the arithmetic of ssm_prefill and enqueues three kernels.
+ *
+ *   every ssm_prefill argument   as for ssm_prefill
+ *   seg_len                      tokens per segment, a positive multiple of 64, giving at
+ *                                most 65535 segments; seg_len >= seqlen is ssm_prefill itself
+ *   workspace, workspace_bytes   device buffer of at least ssm_prefill_workspace_bytes(...)
+ *                                bytes, 16-byte aligned, owned by the caller (NULL allowed
+ *                                for a single segment).  Its contents on entry do not matter;
+ *                                on return they are scratch.  Calls that share a workspace
+ *                                must not overlap on the GPU.
+ * The result depends on seg_len and seqlen, never on d_inner or the launch shape: a
+ * channel slice run with the same seg_len equals the unsplit run bit for bit.  It
+ * differs from ssm_prefill by fp32 rounding only, because the start states are
+ * composed in another order.
+ * Returns SSM_OK or a negative status (SSM_ERR_INVALID_ARG for a bad seg_len or a
+ * missing or short workspace).
+ */
+int ssm_prefill_segmented(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                          ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                          const void* x, const void* z, const void* dt,
+                          int64_t in_stride_b, int64_t in_stride_t,
+                          const void* Bmat, const void* Cmat,
+                          const float* A, const float* Dskip, const float* dt_bias,
+                          const float* conv_w, const float* conv_b,
+                          const float* conv_state_in, const float* ssm_state_in,
+                          int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                          void* out, int64_t out_stride_b, int64_t out_stride_t,
+                          float* conv_state_out, float* ssm_state_out,
+                          int seg_len, void* workspace, size_t workspace_bytes,
+                          void* cuda_stream);
 
 /*
  * ssm_decode_step -- one token per request, continuing from cached states that

@@ -20,8 +20,8 @@ _STATUS = {0: "SSM_OK", -1: "SSM_ERR_INVALID_ARG", -2: "SSM_ERR_UNSUPPORTED", -3
            -4: "SSM_ERR_CUDA", -5: "SSM_ERR_DEVICE_TIMEOUT"}
 DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
 
-EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_decode_step", "ssm_decode_tokens", "q8_reduce_partials",
-           "ssm_device_status", "ssm_last_error")
+EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_segmented",
+           "ssm_decode_step", "ssm_decode_tokens", "q8_reduce_partials", "ssm_device_status", "ssm_last_error")
 
 
 class SSMError(RuntimeError):
@@ -51,6 +51,10 @@ def load(path: Path | str | None = None):
     lib.ssm_prefill.argtypes = [I, I, I, I, I, I, I, P, P, P, L, L, P, P, P, P, P, P, P, P, P, L, L,
                                 P, L, L, P, P, P]
     lib.ssm_prefill.restype = I
+    lib.ssm_prefill_workspace_bytes.argtypes = [I, I, I, I]
+    lib.ssm_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssm_prefill_segmented.argtypes = lib.ssm_prefill.argtypes[:-1] + [I, P, ctypes.c_size_t, P]
+    lib.ssm_prefill_segmented.restype = I
     lib.ssm_decode_step.argtypes = [I, I, I, I, I, I, P, P, P, L, P, P, P, P, P, P, P, P, P, L, L, I, P,
                                     P, L, P]
     lib.ssm_decode_step.restype = I
@@ -118,10 +122,31 @@ def _ssm_state_layout(t, batch, d_inner, name):
     return t.stride(0)
 
 
+def prefill_workspace_bytes(batch: int, seqlen: int, d_inner: int, seg_len: int) -> int:
+    """ssm_prefill_workspace_bytes: device bytes the segmented prefill needs."""
+    return int(load().ssm_prefill_workspace_bytes(batch, seqlen, d_inner, seg_len))
+
+
+def suggest_seg_len(batch: int, seqlen: int, d_inner: int, n_sm: int, ctas_per_sm: int = 3) -> int | None:
+    """A segment length that brings batch x ceil(d_inner/16) x segments close to the GPU's
+    resident CTA slots, or None when the rows already fill it.  The choice depends on
+    d_inner, so channel-slice runs that must match bit for bit pass one seg_len explicitly."""
+    rows = batch * ((d_inner + 15) // 16)
+    slots = n_sm * ctas_per_sm
+    n_seg = min(slots // rows if rows else 1, (seqlen + 63) // 64)
+    if n_seg < 2:
+        return None
+    return ((seqlen + n_seg - 1) // n_seg + 63) // 64 * 64
+
+
 def prefill(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state_in=None, ssm_state_in=None,
-            out=None, out_dtype=torch.float32, conv_state_out=None, ssm_state_out=None, stream=None):
+            out=None, out_dtype=torch.float32, conv_state_out=None, ssm_state_out=None, stream=None,
+            seg_len=None, workspace=None):
     """ssm_prefill over [batch, L, d_inner] x/z/dt (channel-stride-1 views allowed).
 
+    With ``seg_len`` (a multiple of 64) the rows are cut into segments that run in parallel
+    (ssm_prefill_segmented); ``workspace`` is then a CUDA uint8 tensor of at least
+    prefill_workspace_bytes(...) bytes, allocated here with torch when not given.
     Returns (out, conv_state_out, ssm_state_out).
     """
     lib = load()
@@ -154,13 +179,26 @@ def prefill(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state_in=None, s
         raise ValueError("conv_state_in and conv_state_out must share the row stride")
     if ssm_state_in is not None and _ssm_state_layout(ssm_state_in, batch, d_inner, "ssm_state_in") != sb:
         raise ValueError("ssm_state_in and ssm_state_out must share the batch stride")
-    rc = lib.ssm_prefill(batch, L, d_inner, 16, 4, _dtype_code(x.dtype), _dtype_code(out.dtype),
-                         _ptr(x), _ptr(z), _ptr(dt), x.stride(0), x.stride(1), _ptr(B), _ptr(C),
-                         _ptr(A), _ptr(D), _ptr(dt_bias), _ptr(conv_w), _ptr(conv_b),
-                         _ptr(conv_state_in), _ptr(ssm_state_in), ld, sb,
-                         _ptr(out), out.stride(0), out.stride(1),
-                         _ptr(conv_state_out), _ptr(ssm_state_out), _stream(stream))
-    _check(lib, "ssm_prefill", rc)
+    args = (batch, L, d_inner, 16, 4, _dtype_code(x.dtype), _dtype_code(out.dtype),
+            _ptr(x), _ptr(z), _ptr(dt), x.stride(0), x.stride(1), _ptr(B), _ptr(C),
+            _ptr(A), _ptr(D), _ptr(dt_bias), _ptr(conv_w), _ptr(conv_b),
+            _ptr(conv_state_in), _ptr(ssm_state_in), ld, sb,
+            _ptr(out), out.stride(0), out.stride(1),
+            _ptr(conv_state_out), _ptr(ssm_state_out))
+    if seg_len is None:
+        rc = lib.ssm_prefill(*args, _stream(stream))
+        _check(lib, "ssm_prefill", rc)
+        return out, conv_state_out, ssm_state_out
+    need = int(lib.ssm_prefill_workspace_bytes(batch, L, d_inner, int(seg_len)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    if workspace is not None:
+        _need_cuda(workspace)
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.ssm_prefill_segmented(*args, int(seg_len), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(lib, "ssm_prefill_segmented", rc)
     return out, conv_state_out, ssm_state_out
 
 

@@ -2,7 +2,8 @@
 //
 // Every entry point validates its arguments on the host, returns a negative
 // status (with a message for ssm_last_error) before launching anything when they
-// are wrong, and otherwise enqueues exactly one kernel on the caller's stream.
+// are wrong, and otherwise enqueues its kernels on the caller's stream (one
+// kernel; three for a prefill cut into several sequence segments).
 // No entry point allocates memory or keeps per-call state.
 #include <stdarg.h>
 #include <stdio.h>
@@ -56,56 +57,66 @@ int esize(int t) { return t == SSM_BF16 ? 2 : 4; }
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int ssm_abi_version(void) { return 100; }
-
-const char* ssm_last_error(void) { return g_err; }
-
-int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
-                ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
-                const void* x, const void* z, const void* dt,
-                int64_t in_stride_b, int64_t in_stride_t,
-                const void* Bmat, const void* Cmat,
-                const float* A, const float* Dskip, const float* dt_bias,
-                const float* conv_w, const float* conv_b,
-                const float* conv_state_in, const float* ssm_state_in,
-                int64_t conv_state_ld, int64_t ssm_state_stride_b,
-                void* out, int64_t out_stride_b, int64_t out_stride_t,
-                float* conv_state_out, float* ssm_state_out,
-                void* cuda_stream) {
+// Shared by ssm_prefill (one segment) and ssm_prefill_segmented.
+int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                 ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                 const void* x, const void* z, const void* dt,
+                 int64_t in_stride_b, int64_t in_stride_t,
+                 const void* Bmat, const void* Cmat,
+                 const float* A, const float* Dskip, const float* dt_bias,
+                 const float* conv_w, const float* conv_b,
+                 const float* conv_state_in, const float* ssm_state_in,
+                 int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                 void* out, int64_t out_stride_b, int64_t out_stride_t,
+                 float* conv_state_out, float* ssm_state_out,
+                 int seg_len, void* workspace, size_t workspace_bytes,
+                 void* cuda_stream) {
     g_err[0] = 0;
-    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: batch %lld not in [1, 65535]", (long long)(batch));
-    if (seqlen < 1 || seqlen > (1 << 30)) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: seqlen %lld not in [1, 2^30]", (long long)(seqlen));
-    if (d_inner < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: d_inner %lld < 1", (long long)(d_inner));
-    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: unknown dtype");
-    if (d_state != 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_prefill: d_state %lld unsupported (16 only)", (long long)(d_state));
-    if (d_conv != 4) return fail(SSM_ERR_UNSUPPORTED, "ssm_prefill: d_conv %lld unsupported (4 only)", (long long)(d_conv));
-    if (d_inner % 8 != 0) return fail(SSM_ERR_UNSUPPORTED, "ssm_prefill: d_inner %lld is not a multiple of 8", (long long)(d_inner));
+    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: batch %lld not in [1, 65535]", fn, (long long)(batch));
+    if (seqlen < 1 || seqlen > (1 << 30)) return fail(SSM_ERR_INVALID_ARG, "%s: seqlen %lld not in [1, 2^30]", fn, (long long)(seqlen));
+    if (d_inner < 1) return fail(SSM_ERR_INVALID_ARG, "%s: d_inner %lld < 1", fn, (long long)(d_inner));
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (d_state != 16) return fail(SSM_ERR_UNSUPPORTED, "%s: d_state %lld unsupported (16 only)", fn, (long long)(d_state));
+    if (d_conv != 4) return fail(SSM_ERR_UNSUPPORTED, "%s: d_conv %lld unsupported (4 only)", fn, (long long)(d_conv));
+    if (d_inner % 8 != 0) return fail(SSM_ERR_UNSUPPORTED, "%s: d_inner %lld is not a multiple of 8", fn, (long long)(d_inner));
     if (!x || !z || !dt || !Bmat || !Cmat || !A || !Dskip || !dt_bias || !conv_w || !conv_b || !out ||
         !conv_state_out || !ssm_state_out)
-        return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: a required pointer is NULL");
-    if (in_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: in_stride_t %lld < d_inner", (long long)(in_stride_t));
-    if (batch > 1 && in_stride_b < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: in_stride_b %lld < 1", (long long)(in_stride_b));
-    if (out_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: out_stride_t %lld < d_inner", (long long)(out_stride_t));
+        return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (in_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "%s: in_stride_t %lld < d_inner", fn, (long long)(in_stride_t));
+    if (batch > 1 && in_stride_b < 1) return fail(SSM_ERR_INVALID_ARG, "%s: in_stride_b %lld < 1", fn, (long long)(in_stride_b));
+    if (out_stride_t < d_inner) return fail(SSM_ERR_INVALID_ARG, "%s: out_stride_t %lld < d_inner", fn, (long long)(out_stride_t));
     if (batch > 1 && out_stride_b < (int64_t)(seqlen - 1) * out_stride_t + d_inner)
-        return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: out_stride_b %lld lets batch rows overlap", (long long)(out_stride_b));
-    if (conv_state_ld < d_inner) return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: conv_state_ld %lld < d_inner", (long long)(conv_state_ld));
+        return fail(SSM_ERR_INVALID_ARG, "%s: out_stride_b %lld lets batch rows overlap", fn, (long long)(out_stride_b));
+    if (conv_state_ld < d_inner) return fail(SSM_ERR_INVALID_ARG, "%s: conv_state_ld %lld < d_inner", fn, (long long)(conv_state_ld));
     if (ssm_state_stride_b < 16LL * d_inner)
-        return fail(SSM_ERR_INVALID_ARG, "ssm_prefill: ssm_state_stride_b %lld < 16*d_inner", (long long)(ssm_state_stride_b));
+        return fail(SSM_ERR_INVALID_ARG, "%s: ssm_state_stride_b %lld < 16*d_inner", fn, (long long)(ssm_state_stride_b));
     const int es = esize(in_dtype);
     if (!aligned(x, 16) || !aligned(z, 16) || !aligned(dt, 16) || !aligned(Bmat, 16) || !aligned(Cmat, 16))
-        return fail(SSM_ERR_MISALIGNED, "ssm_prefill: x, z, dt, B and C must be 16-byte aligned");
+        return fail(SSM_ERR_MISALIGNED, "%s: x, z, dt, B and C must be 16-byte aligned", fn);
     if ((in_stride_t * es) % 16 != 0 || (batch > 1 && (in_stride_b * es) % 16 != 0))
-        return fail(SSM_ERR_MISALIGNED, "ssm_prefill: input strides must be multiples of 16 bytes");
-    if (!aligned(A, 16) || !aligned(conv_w, 16)) return fail(SSM_ERR_MISALIGNED, "ssm_prefill: A and conv_w must be 16-byte aligned");
+        return fail(SSM_ERR_MISALIGNED, "%s: input strides must be multiples of 16 bytes", fn);
+    if (!aligned(A, 16) || !aligned(conv_w, 16)) return fail(SSM_ERR_MISALIGNED, "%s: A and conv_w must be 16-byte aligned", fn);
     if (!aligned(ssm_state_out, 8) || (ssm_state_in && !aligned(ssm_state_in, 8)) || ssm_state_stride_b % 2 != 0)
-        return fail(SSM_ERR_MISALIGNED, "ssm_prefill: ssm states must be 8-byte aligned with an even batch stride");
-    if (!aligned(out, esize(out_dtype))) return fail(SSM_ERR_MISALIGNED, "ssm_prefill: out is not element aligned");
+        return fail(SSM_ERR_MISALIGNED, "%s: ssm states must be 8-byte aligned with an even batch stride", fn);
+    if (!aligned(out, esize(out_dtype))) return fail(SSM_ERR_MISALIGNED, "%s: out is not element aligned", fn);
+    if (seg_len < ssm::kPrefillChunk || seg_len % ssm::kPrefillChunk != 0)
+        return fail(SSM_ERR_INVALID_ARG, "%s: seg_len %lld is not a positive multiple of %d", fn, (long long)seg_len,
+                    ssm::kPrefillChunk);
+    const int64_t n_seg = ((int64_t)seqlen + seg_len - 1) / seg_len;
+    if (n_seg > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: %lld segments (at most 65535)", fn, (long long)n_seg);
+    if (n_seg > 1) {
+        const size_t need = ssm_prefill_workspace_bytes(batch, seqlen, d_inner, seg_len);
+        if (!workspace || workspace_bytes < need)
+            return fail(SSM_ERR_INVALID_ARG, "%s: workspace of %zu bytes given, %zu needed", fn,
+                        workspace ? workspace_bytes : (size_t)0, need);
+        if (!aligned(workspace, 16)) return fail(SSM_ERR_MISALIGNED, "%s: workspace must be 16-byte aligned", fn);
+    }
 
     int serr = 0;
     unsigned int* status = status_ptr(&serr);
-    if (serr) return fail(SSM_ERR_CUDA, "ssm_prefill: no usable CUDA device");
+    if (serr) return fail(SSM_ERR_CUDA, "%s: no usable CUDA device", fn);
 
     ssm::PrefillLaunch q{};
     q.batch = batch;
@@ -136,10 +147,70 @@ int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
     a.conv_state_out = conv_state_out;
     a.ssm_state_out = ssm_state_out;
     a.status = status;
+    a.seg_len = n_seg > 1 ? seg_len : seqlen;
+    a.n_seg = (int)n_seg;
+    a.ws = n_seg > 1 ? static_cast<float*>(workspace) : nullptr;
     const char* why = "";
     if (ssm::launch_prefill(q, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
-        return fail(SSM_ERR_CUDA, "ssm_prefill: %s", why);
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
     return SSM_OK;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+int ssm_abi_version(void) { return 101; }
+
+const char* ssm_last_error(void) { return g_err; }
+
+int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                const void* x, const void* z, const void* dt,
+                int64_t in_stride_b, int64_t in_stride_t,
+                const void* Bmat, const void* Cmat,
+                const float* A, const float* Dskip, const float* dt_bias,
+                const float* conv_w, const float* conv_b,
+                const float* conv_state_in, const float* ssm_state_in,
+                int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                void* out, int64_t out_stride_b, int64_t out_stride_t,
+                float* conv_state_out, float* ssm_state_out,
+                void* cuda_stream) {
+    // one segment covering the whole row (seg_len rounded up to whole chunks)
+    const int one = seqlen > 0 && seqlen <= (1 << 30)
+                        ? (seqlen + ssm::kPrefillChunk - 1) / ssm::kPrefillChunk * ssm::kPrefillChunk
+                        : ssm::kPrefillChunk;
+    return prefill_impl("ssm_prefill", batch, seqlen, d_inner, d_state, d_conv, in_dtype, out_dtype, x, z, dt,
+                        in_stride_b, in_stride_t, Bmat, Cmat, A, Dskip, dt_bias, conv_w, conv_b, conv_state_in,
+                        ssm_state_in, conv_state_ld, ssm_state_stride_b, out, out_stride_b, out_stride_t,
+                        conv_state_out, ssm_state_out, one, nullptr, 0, cuda_stream);
+}
+
+size_t ssm_prefill_workspace_bytes(int batch, int seqlen, int d_inner, int seg_len) {
+    if (batch < 1 || seqlen < 1 || d_inner < 1 || seg_len < 1) return 0;
+    const int64_t n_seg = ((int64_t)seqlen + seg_len - 1) / seg_len;
+    return (size_t)(n_seg - 1) * (size_t)batch * (size_t)d_inner * 32 * sizeof(float);
+}
+
+int ssm_prefill_segmented(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                          ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                          const void* x, const void* z, const void* dt,
+                          int64_t in_stride_b, int64_t in_stride_t,
+                          const void* Bmat, const void* Cmat,
+                          const float* A, const float* Dskip, const float* dt_bias,
+                          const float* conv_w, const float* conv_b,
+                          const float* conv_state_in, const float* ssm_state_in,
+                          int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                          void* out, int64_t out_stride_b, int64_t out_stride_t,
+                          float* conv_state_out, float* ssm_state_out,
+                          int seg_len, void* workspace, size_t workspace_bytes,
+                          void* cuda_stream) {
+    return prefill_impl("ssm_prefill_segmented", batch, seqlen, d_inner, d_state, d_conv, in_dtype, out_dtype,
+                        x, z, dt, in_stride_b, in_stride_t, Bmat, Cmat, A, Dskip, dt_bias, conv_w, conv_b,
+                        conv_state_in, ssm_state_in, conv_state_ld, ssm_state_stride_b, out, out_stride_b,
+                        out_stride_t, conv_state_out, ssm_state_out, seg_len, workspace, workspace_bytes,
+                        cuda_stream);
 }
 
 }  // extern "C"

@@ -62,6 +62,17 @@ __device__ __forceinline__ float softplus(float v) {
     return v > 20.0f ? v : (e < 0.0625f ? series : viaLog);
 }
 
+// The per-token activations, chosen by the precision of the token inputs.
+//   bf16 inputs: the MUFU forms above; their few-ulp error is far below the resolution of
+//                a bf16 input.
+//   fp32 inputs: CUDA's expf and log1pf with IEEE division.  Outputs of the mixer reach
+//                tens of times their RMS and carry the relative error of u and delta
+//                through the state sum, so the fp32 path keeps these to a few ulp.
+template <typename Tin> __device__ __forceinline__ float silu_in(float x) { return silu(x); }
+template <> __device__ __forceinline__ float silu_in<float>(float x) { return __fdiv_rn(x, 1.0f + expf(-x)); }
+template <typename Tin> __device__ __forceinline__ float softplus_in(float v) { return softplus(v); }
+template <> __device__ __forceinline__ float softplus_in<float>(float v) { return v > 20.0f ? v : log1pf(expf(v)); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -81,8 +81,8 @@ k_decode(const DecodeArgs p) {
         c0 = c1;
         c1 = c2;
         c2 = xt;
-        const float u = silu(xc);
-        const float delta = softplus(dtt + bias);
+        const float u = silu_in<Tin>(xc);
+        const float delta = softplus_in<Tin>(dtt + bias);
         const float du = delta * u;
         float y = 0.f;
 #pragma unroll
@@ -102,7 +102,7 @@ k_decode(const DecodeArgs p) {
         }
         y = fmaf(Dd, u, y);
         reinterpret_cast<Tout*>(p.out)[(int64_t)r * p.out_stride_b + (int64_t)t * p.out_stride_t + d] =
-            from_f32<Tout>(y * silu(zt));
+            from_f32<Tout>(y * silu_in<Tin>(zt));
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) hp[q] = h[q];

@@ -19,6 +19,12 @@ struct PrefillArgs {
     int64_t out_stride_b, out_stride_t;
     float *conv_state_out, *ssm_state_out;
     unsigned int* status;
+    // Sequence segments: tokens [g*seg_len, min(L, (g+1)*seg_len)) of every row form segment g
+    // (seg_len = seqlen and n_seg = 1 when unsegmented).  ws holds, per earlier segment g < n_seg-1
+    // and (b, d), 32 floats: the segment's state from zero (then the next segment's start state)
+    // and the product of its decays.
+    int seg_len, n_seg;
+    float* ws;
 };
 
 struct PrefillLaunch {
@@ -41,6 +47,9 @@ struct DecodeArgs {
     int64_t out_stride_b, out_stride_t;
     unsigned int* status;
 };
+
+// Tokens per prefill chunk; a sequence segment is a whole number of chunks.
+constexpr int kPrefillChunk = 64;
 
 constexpr int kMaxPartials = 8;
 

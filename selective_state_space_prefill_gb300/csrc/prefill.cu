@@ -112,7 +112,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const int d = d0 + c;
     const bool dvalid = d < p.d_inner;
     const int L = p.seqlen;
-    const int n_iter = (L + TC - 1) / TC;
+    // sequence segment blockIdx.z: tokens [blockIdx.z * seg_len, min(L, (blockIdx.z + 1) * seg_len))
+    const int n_iter = (min(L - (int)blockIdx.z * p.seg_len, p.seg_len) + TC - 1) / TC;
 
     // TMA destinations need 128-byte alignment; refuse (and report) rather than fault.
     if (smem_u32(smem) & 127u) {
@@ -133,7 +134,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     auto issue = [&](int it) {
         const int s = it % kStages;
         unsigned char* st = smem + s * Lay::STAGE;
-        const int t0 = it * TC;
+        const int t0 = (int)blockIdx.z * p.seg_len + it * TC;
         mbar_arrive_expect_tx(&full[s], Lay::TX);
         tma_load_3d(st + Lay::OFF_X, &tm_x, &full[s], d0, t0 - 3, b);
         tma_load_3d(st + Lay::OFF_Z, &tm_z, &full[s], d0, t0, b);
@@ -168,7 +169,13 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         cb = __ldg(p.conv_b + d);
         Dd = __ldg(p.Dskip + d);
         bias = __ldg(p.dt_bias + d);
-        if (p.ssm_state_in) {
+        if (blockIdx.z > 0) {
+            // the start state of this segment, left in the workspace by the carry pass
+            const float2* hs = reinterpret_cast<const float2*>(
+                p.ws + (((int64_t)(blockIdx.z - 1) * gridDim.y + b) * p.d_inner + d) * 32 + 8 * g);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) carry[q] = hs[q];
+        } else if (p.ssm_state_in) {
             const float2* hs = reinterpret_cast<const float2*>(
                 p.ssm_state_in + (int64_t)b * p.ssm_state_stride_b + (int64_t)d * kN + 8 * g);
 #pragma unroll
@@ -211,12 +218,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         // ---- per-token work for this lane's half of the warp's K tokens:
         //      conv + SiLU, softplus step, skip term
         const int row0 = warp * K;            // first token of this warp in the chunk
-        const int tbase = it * TC + row0;     // its absolute index
+        const int tbase = (int)blockIdx.z * p.seg_len + it * TC + row0;   // its absolute index
         const int r0 = row0 + KH * g;         // first token this lane computes
         float xm3 = to_f32(xs[(r0 + 0) * kCD + c]);   // x[t-3] (tile row 0 = chunk start - 3)
         float xm2 = to_f32(xs[(r0 + 1) * kCD + c]);
         float xm1 = to_f32(xs[(r0 + 2) * kCD + c]);
-        if (it == 0 && warp == 0 && g == 0 && p.conv_state_in != nullptr && dvalid) {
+        if (it == 0 && blockIdx.z == 0 && warp == 0 && g == 0 && p.conv_state_in != nullptr && dvalid) {
             const float* cs = p.conv_state_in + (int64_t)b * 3 * p.conv_state_ld + d;
             xm3 = cs[0];
             xm2 = cs[p.conv_state_ld];
@@ -232,8 +239,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             xc = fmaf(w2, xm1, xc);
             xc = fmaf(w3, xt, xc);
             xm3 = xm2; xm2 = xm1; xm1 = xt;
-            const float u = silu(xc);
-            float delta = softplus(to_f32(dts[(r0 + k) * kCD + c]) + bias);
+            const float u = silu_in<Tin>(xc);
+            float delta = softplus_in<Tin>(to_f32(dts[(r0 + k) * kCD + c]) + bias);
             if (tbase + KH * g + k >= L) delta = 0.f;   // padding rows: a = 1, b = 0 (identity)
             dl_own[k] = delta;
             du_own[k] = delta * u;
@@ -305,15 +312,15 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const int t = t_own + k;
             if (dvalid && t < L) {
                 const float yv = (mine + other) + ud[k];
-                const float gz = silu(to_f32(zs[(r0 + k) * kCD + c]));
+                const float gz = silu_in<Tin>(to_f32(zs[(r0 + k) * kCD + c]));
                 reinterpret_cast<Tout*>(p.out)[(int64_t)b * p.out_stride_b + (int64_t)t * p.out_stride_t + d] =
                     from_f32<Tout>(yv * gz);
             }
         }
     }
 
-    // ---- final states: h_L and the last three raw inputs
-    if (warp == 0 && dvalid) {
+    // ---- final states (last segment): h_L and the last three raw inputs
+    if ((int)blockIdx.z == p.n_seg - 1 && warp == 0 && dvalid) {
         float2* hs = reinterpret_cast<float2*>(p.ssm_state_out + (int64_t)b * p.ssm_state_stride_b +
                                                (int64_t)d * kN + 8 * g);
 #pragma unroll
@@ -333,6 +340,229 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 co[(int64_t)k * p.conv_state_ld] = v;
             }
         }
+    }
+}
+
+// ------------------------------------------------------------------ segmented prefill
+// Long rows with few (batch x channel-group) CTAs leave most SMs idle, so the sequence
+// can be cut into segments that run in parallel: the recurrence composes, and the
+// pair (prod_t a_t, state from zero) of a segment carries it from its start state to
+// its end state.  Pass A computes that pair for every segment but the last; pass B
+// walks the segments of each (b, d, n) in order and turns the pairs into start
+// states; pass C is k_prefill, each segment starting from its start state.
+
+template <int S, int K, typename Tin>
+struct AggLayout {
+    static constexpr int TC = S * K;
+    static constexpr int ES = (int)sizeof(Tin);
+    static constexpr int X_BYTES = (TC + 3) * kCD * ES;
+    static constexpr int DT_BYTES = TC * kCD * ES;
+    static constexpr int B_BYTES = TC * kN * ES;
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_DT = align128(OFF_X + X_BYTES);
+    static constexpr int OFF_B = align128(OFF_DT + DT_BYTES);
+    static constexpr int STAGE = align128(OFF_B + B_BYTES);
+    static constexpr int TX = X_BYTES + DT_BYTES + B_BYTES;
+    static constexpr int OFF_BF = kStages * STAGE;           // fp32 B of the chunk, [TC][16]
+    static constexpr int OFF_XCH = OFF_BF + TC * kN * 4;     // [4 pairs][S][32] float4
+    static constexpr int OFF_BAR = OFF_XCH + 4 * S * 32 * 16;
+    static constexpr int TOTAL = OFF_BAR + kStages * 8;
+};
+
+// Pass A: segment sg (< n_seg - 1, always a whole number of chunks) of 16 channels of
+// row b: the state reached from zero and the product of the decays, into ws.
+template <int S, int K, typename Tin>
+__global__ void __launch_bounds__(S * 32, 3)
+k_prefill_agg(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
+              const __grid_constant__ CUtensorMap tm_B, const PrefillArgs p) {
+    using Lay = AggLayout<S, K, Tin>;
+    constexpr int TC = Lay::TC;
+    constexpr int KH = K / 2;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* Bf = reinterpret_cast<float*>(smem + Lay::OFF_BF);
+    float4* xch = reinterpret_cast<float4*>(smem + Lay::OFF_XCH);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::OFF_BAR);
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int c = lane & 15;
+    const int g = lane >> 4;
+    const int d0 = blockIdx.x * kCD;
+    const int b = blockIdx.y;
+    const int sg = blockIdx.z;
+    const int d = d0 + c;
+    const bool dvalid = d < p.d_inner;
+    const int T0 = sg * p.seg_len;
+    const int n_iter = p.seg_len / TC;
+
+    if (smem_u32(smem) & 127u) {
+        if (threadIdx.x == 0) atomicOr(p.status, 4u);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_dt);
+        prefetch_tmap(&tm_B);
+    }
+    __syncthreads();
+
+    auto issue = [&](int it) {
+        const int s = it % kStages;
+        unsigned char* st = smem + s * Lay::STAGE;
+        const int t0 = T0 + it * TC;
+        mbar_arrive_expect_tx(&full[s], Lay::TX);
+        tma_load_3d(st + Lay::OFF_X, &tm_x, &full[s], d0, t0 - 3, b);
+        tma_load_3d(st + Lay::OFF_DT, &tm_dt, &full[s], d0, t0, b);
+        tma_load_3d(st + Lay::OFF_B, &tm_B, &full[s], 0, t0, b);
+    };
+    if (threadIdx.x == 0) {
+        for (int it = 0; it < kStages - 1 && it < n_iter; ++it) issue(it);
+    }
+
+    float A2[8];
+    float bias = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f, cb = 0.f;
+    float2 carry[4], decay[4];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) A2[m] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        carry[q] = f2(0.f, 0.f);
+        decay[q] = f2(1.f, 1.f);
+    }
+    if (dvalid) {
+        const float4* Ar = reinterpret_cast<const float4*>(p.A + (int64_t)d * kN + 8 * g);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float4 v = __ldg(Ar + q);
+            A2[4 * q + 0] = v.x * kLog2e;
+            A2[4 * q + 1] = v.y * kLog2e;
+            A2[4 * q + 2] = v.z * kLog2e;
+            A2[4 * q + 3] = v.w * kLog2e;
+        }
+        const float4 w = __ldg(reinterpret_cast<const float4*>(p.conv_w + (int64_t)d * 4));
+        w0 = w.x; w1 = w.y; w2 = w.z; w3 = w.w;
+        cb = __ldg(p.conv_b + d);
+        bias = __ldg(p.dt_bias + d);
+    }
+
+    for (int it = 0; it < n_iter; ++it) {
+        const int s = it % kStages;
+        const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((it / kStages) & 1));
+        const unsigned char* st = smem + s * Lay::STAGE;
+        const Tin* xs = reinterpret_cast<const Tin*>(st + Lay::OFF_X);
+        const Tin* dts = reinterpret_cast<const Tin*>(st + Lay::OFF_DT);
+        if (ok) {
+            // the previous chunk's readers of Bf all passed its exchange barrier
+            const Tin* Bs = reinterpret_cast<const Tin*>(st + Lay::OFF_B);
+#pragma unroll
+            for (int e = 2 * threadIdx.x; e < TC * kN; e += 2 * S * 32)
+                *reinterpret_cast<float2*>(Bf + e) = load_pair(Bs + e);
+        }
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) {
+                atomicOr(p.status, 1u);
+                for (int j = it; j < n_iter && j < it + kStages - 1; ++j)
+                    (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1), 100000000ull);
+            }
+            return;
+        }
+        // every warp has finished chunk it-1, so its stage can be refilled
+        if (threadIdx.x == 0 && it + kStages - 1 < n_iter) issue(it + kStages - 1);
+
+        const int row0 = warp * K;
+        const int r0 = row0 + KH * g;
+        float xm3 = to_f32(xs[(r0 + 0) * kCD + c]);
+        float xm2 = to_f32(xs[(r0 + 1) * kCD + c]);
+        float xm1 = to_f32(xs[(r0 + 2) * kCD + c]);
+        if (it == 0 && sg == 0 && warp == 0 && g == 0 && p.conv_state_in != nullptr && dvalid) {
+            const float* cs = p.conv_state_in + (int64_t)b * 3 * p.conv_state_ld + d;
+            xm3 = cs[0];
+            xm2 = cs[p.conv_state_ld];
+            xm1 = cs[2 * p.conv_state_ld];
+        }
+        float dl_own[KH], du_own[KH];
+        float dsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < KH; ++k) {
+            const float xt = to_f32(xs[(r0 + k + 3) * kCD + c]);
+            float xc = fmaf(w0, xm3, cb);
+            xc = fmaf(w1, xm2, xc);
+            xc = fmaf(w2, xm1, xc);
+            xc = fmaf(w3, xt, xc);
+            xm3 = xm2; xm2 = xm1; xm1 = xt;
+            const float u = silu_in<Tin>(xc);
+            const float delta = softplus_in<Tin>(to_f32(dts[(r0 + k) * kCD + c]) + bias);
+            dl_own[k] = delta;
+            du_own[k] = delta * u;
+            dsum += delta;
+        }
+        float dl[K], du[K];
+#pragma unroll
+        for (int k = 0; k < KH; ++k) {
+            dl[k] = __shfl_sync(0xffffffffu, dl_own[k], c);
+            dl[KH + k] = __shfl_sync(0xffffffffu, dl_own[k], c + 16);
+            du[k] = __shfl_sync(0xffffffffu, du_own[k], c);
+            du[KH + k] = __shfl_sync(0xffffffffu, du_own[k], c + 16);
+        }
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, 16);
+
+        // sub-chunk aggregates of all four state pairs, then one exchange
+        const float* bw = Bf + row0 * kN + 8 * g;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float2 Ap = f2(A2[2 * r], A2[2 * r + 1]);
+            float2 agg = f2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const float2 e = __fmul2_rn(f2(dl[i], dl[i]), Ap);
+                const float2 a = f2(ex2(e.x), ex2(e.y));
+                const float2 Bi = *reinterpret_cast<const float2*>(bw + i * kN + 2 * r);
+                agg = __ffma2_rn(a, agg, __fmul2_rn(f2(du[i], du[i]), Bi));
+            }
+            const float2 ea = __fmul2_rn(f2(dsum, dsum), Ap);
+            xch[(r * S + warp) * 32 + lane] = make_float4(ex2(ea.x), ex2(ea.y), agg.x, agg.y);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float2 h = carry[r], dec = decay[r];
+#pragma unroll
+            for (int j = 0; j < S; ++j) {
+                const float4 e = xch[(r * S + j) * 32 + lane];
+                h = __ffma2_rn(f2(e.x, e.y), h, f2(e.z, e.w));
+                dec = __fmul2_rn(dec, f2(e.x, e.y));
+            }
+            carry[r] = h;
+            decay[r] = dec;
+        }
+    }
+    if (dvalid) {
+        float2* w = reinterpret_cast<float2*>(p.ws + (((int64_t)sg * gridDim.y + b) * p.d_inner + d) * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w[4 * g + q] = carry[q];          // states 8g .. 8g+7
+            w[8 + 4 * g + q] = decay[q];      // their decay products
+        }
+    }
+}
+
+// Pass B: one thread per (b, d, n) folds the segments in order; entry sg of ws then holds the
+// start state of segment sg + 1 in place of segment sg's state from zero.
+__global__ void __launch_bounds__(256)
+k_prefill_carry(const PrefillArgs p, int batch) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;      // (b, d, n)
+    const int64_t per_row = (int64_t)p.d_inner * kN;
+    if (i >= batch * per_row) return;
+    const int64_t b = i / per_row;
+    const int64_t dn = i - b * per_row;
+    const int64_t d = dn / kN, n = dn - d * kN;
+    float h = p.ssm_state_in ? p.ssm_state_in[b * p.ssm_state_stride_b + dn] : 0.f;
+    for (int sg = 0; sg < p.n_seg - 1; ++sg) {
+        float* w = p.ws + (((int64_t)sg * batch + b) * p.d_inner + d) * 32;
+        h = fmaf(w[16 + n], h, w[n]);
+        w[n] = h;
     }
 }
 
@@ -365,6 +595,24 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t
     return r == CUDA_SUCCESS;
 }
 
+// The dynamic shared-memory opt-in is per function and device; *done remembers it per device.
+template <typename F>
+bool opt_in_smem(F* kern, int bytes, unsigned long long* done, const char** why) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        *why = "cudaGetDevice failed";
+        return false;
+    }
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+        return false;
+    }
+    __atomic_fetch_or(done, bit, __ATOMIC_ACQ_REL);
+    return true;
+}
+
 template <int S, int K, typename Tin, typename Tout>
 int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
     using Lay = Layout<S, K, Tin>;
@@ -385,25 +633,26 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
         return -1;
     }
-    auto kern = k_prefill<S, K, Tin, Tout>;
-    // The shared-memory opt-in is per function and device; remember it per device.
-    static unsigned long long attr_done = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        *why = "cudaGetDevice failed";
-        return -1;
-    }
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL) !=
-            cudaSuccess) {
-            *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+    const unsigned gx = (unsigned)((a.d_inner + kCD - 1) / kCD);
+    if (a.n_seg > 1) {
+        // pass A (segments 0 .. n_seg-2), then pass B
+        using ALay = AggLayout<S, K, Tin>;
+        static unsigned long long agg_attr = 0;
+        auto kagg = k_prefill_agg<S, K, Tin>;
+        if (!opt_in_smem(kagg, ALay::TOTAL, &agg_attr, why)) return -1;
+        kagg<<<dim3(gx, q.batch, a.n_seg - 1), S * 32, ALay::TOTAL, stream>>>(mx, mdt, mB, a);
+        const int64_t n = (int64_t)q.batch * a.d_inner * kN;
+        k_prefill_carry<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a, q.batch);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            *why = cudaGetErrorString(e);
             return -1;
         }
-        __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
     }
-    dim3 grid((a.d_inner + kCD - 1) / kCD, q.batch);
-    kern<<<grid, S * 32, Lay::TOTAL, stream>>>(mx, mz, mdt, mB, mC, a);
+    static unsigned long long attr = 0;
+    auto kern = k_prefill<S, K, Tin, Tout>;
+    if (!opt_in_smem(kern, Lay::TOTAL, &attr, why)) return -1;
+    kern<<<dim3(gx, q.batch, a.n_seg), S * 32, Lay::TOTAL, stream>>>(mx, mz, mdt, mB, mC, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
@@ -417,6 +666,7 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
 // Compile-time split of a chunk: S warps x K tokens.
 constexpr int kS = 4;
 constexpr int kK = 16;
+static_assert(kS * kK == kPrefillChunk, "segments are whole chunks");
 
 int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
     if (q.in_bf16) {

@@ -8,9 +8,10 @@ import oracle
 from selective_state_space_prefill_gb300 import binding as ssm
 from selective_state_space_prefill_gb300.inputs import MixerInputs
 
-# Tolerances: max |gpu - oracle| <= TOL * RMS(oracle) per output tensor.
-TOL_BF16 = 2e-3   # bf16 token inputs, fp32 state
-TOL_F32 = 1e-5    # all-fp32 inputs
+# Tolerances.  bf16 token inputs (fp32 state): max |gpu - oracle| <= 2e-3 * RMS(oracle) per
+# output tensor.  All-fp32 inputs: |gpu - oracle| <= 1e-5 * max(|oracle|, RMS(oracle)) per element.
+TOL_BF16 = 2e-3
+TOL_F32 = 1e-5
 
 
 def tol_for(dtype) -> float:
@@ -27,6 +28,30 @@ def assert_rms_close(got, ref, tol, what="", extra=None):
     worst = float(np.max(err - bound)) if np.ndim(bound) else float(np.max(err)) - bound
     assert worst <= 0.0, f"{what}: max|err| {float(np.max(err)):.3e} vs tol {tol:g} * rms {rms:.3e}"
     return float(np.max(err)) / max(rms, 1e-300)
+
+
+def assert_rel_close(got, ref, tol, what=""):
+    """Per-element relative error with an RMS floor: |err_i| <= tol * max(|ref_i|, RMS(ref)).
+    The reading of "1e-5 relative" for all-fp32 inputs: relative error of each element, and
+    near a zero crossing (where relative error has no meaning) the tensor's RMS instead."""
+    got = np.asarray(got.detach().cpu().double().numpy() if isinstance(got, torch.Tensor) else got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, f"{what}: shape {got.shape} vs {ref.shape}"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    scale = np.maximum(np.abs(ref), rms)
+    rel = np.abs(got - ref) / np.maximum(scale, 1e-300)
+    k = int(np.argmax(rel))
+    assert rel.flat[k] <= tol, (f"{what}: error {float(np.abs(got - ref).flat[k]):.3e} at |ref| "
+                                f"{float(np.abs(ref).flat[k]):.3e} (rms {rms:.3e}) is {float(rel.flat[k]):.3e} > {tol:g}")
+    return float(rel.flat[k])
+
+
+def assert_parity(got, ref, dtype, what=""):
+    """The parity bar by input precision: bf16 inputs max|err| <= 2e-3 * RMS; fp32 inputs
+    relative error <= 1e-5 per element with an RMS floor."""
+    if dtype == torch.bfloat16:
+        return assert_rms_close(got, ref, TOL_BF16, what)
+    return assert_rel_close(got, ref, TOL_F32, what)
 
 
 def half_ulp_bf16(ref):

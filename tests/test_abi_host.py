@@ -26,7 +26,7 @@ def lib():
 
 def declared_functions():
     text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
-    return sorted(set(re.findall(r"^(?:int|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^(?:int|size_t|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_three_calls():
@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding.EXPORTS)
     for fn in names:
         assert hasattr(lib, fn), fn
-    assert lib.ssm_abi_version() == 100
+    assert lib.ssm_abi_version() == 101
 
 
 FAKE = 0x10000  # 64 KiB-aligned fake device address, never dereferenced
@@ -125,3 +125,51 @@ def _tokens(lib, **kw):
 def test_decode_tokens_rejects_bad_arguments(lib, kw, code):
     assert _tokens(lib, **kw) == code
     assert lib.ssm_last_error().decode().startswith("ssm_decode_tokens")
+
+
+def _segmented(lib, seg_len=64, ws=FAKE, ws_bytes=1 << 20, **kw):
+    a = dict(batch=2, seqlen=200, d_inner=64, d_state=16, d_conv=4, in_dtype=1, out_dtype=0,
+             x=FAKE, z=FAKE, dt=FAKE, in_stride_b=200 * 64, in_stride_t=64, B=FAKE, C=FAKE, A=FAKE,
+             D=FAKE, dt_bias=FAKE, conv_w=FAKE, conv_b=FAKE, csi=None, ssi=None, ld=64, sb=64 * 16,
+             out=FAKE, ob=200 * 64, ot=64, cso=FAKE, sso=FAKE)
+    a.update(kw)
+    return lib.ssm_prefill_segmented(*a.values(), seg_len, ws, ws_bytes, None)
+
+
+def test_prefill_workspace_bytes(lib):
+    # (ceil(L / seg_len) - 1) segments x batch x d_inner x 32 floats
+    assert lib.ssm_prefill_workspace_bytes(2, 200, 64, 64) == 3 * 2 * 64 * 128
+    assert lib.ssm_prefill_workspace_bytes(1, 16384, 2048, 4096) == 3 * 2048 * 128
+    assert lib.ssm_prefill_workspace_bytes(4, 128, 64, 128) == 0          # one segment
+    assert lib.ssm_prefill_workspace_bytes(4, 128, 64, 4096) == 0
+    assert lib.ssm_prefill_workspace_bytes(0, 128, 64, 64) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(seg_len=0), INVALID), (dict(seg_len=96), INVALID), (dict(seg_len=-64), INVALID),
+    (dict(ws=None), INVALID), (dict(ws_bytes=3 * 2 * 64 * 128 - 1), INVALID),
+    (dict(ws=FAKE + 8), MISALIGNED), (dict(batch=0), INVALID), (dict(d_state=8), UNSUPPORTED),
+    (dict(seqlen=64 * 65536, in_stride_b=0, batch=1, ob=0), INVALID),     # 65536 segments
+])
+def test_prefill_segmented_rejects_bad_arguments(lib, kw, code):
+    assert _segmented(lib, **kw) == code
+    assert lib.ssm_last_error().decode().startswith("ssm_prefill_segmented")
+
+
+def test_prefill_segmented_single_segment_needs_no_workspace(lib):
+    """seg_len >= seqlen is the plain prefill: no workspace, and a valid call on a machine
+    without a GPU fails with SSM_ERR_CUDA only after validation."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _segmented(lib, seg_len=256, ws=None, ws_bytes=0) == CUDA
+    assert _segmented(lib, seg_len=64, ws=FAKE, ws_bytes=3 * 2 * 64 * 128) == CUDA
+
+
+def test_suggest_seg_len():
+    # 96 channel groups x 1 row on 152 SMs x 3 slots: 4 segments of 512 tokens
+    assert binding.suggest_seg_len(1, 2048, 1536, 152) == 512
+    assert binding.suggest_seg_len(4, 2048, 1536, 152) is None           # 384 CTAs already
+    assert binding.suggest_seg_len(1, 16384, 2048, 152) == 5504          # 3 segments
+    assert binding.suggest_seg_len(1, 100, 64, 152) == 64
+    assert binding.suggest_seg_len(1, 64, 64, 152) is None               # a single chunk
