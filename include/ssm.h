@@ -161,6 +161,47 @@ int ssm_prefill_segmented(int batch, int seqlen, int d_inner, int d_state, int d
                           int seg_len, void* workspace, size_t workspace_bytes,
                           void* cuda_stream);
 
+/* Size of the fixed scratch array behind ssm_prefill_segmented_noalloc: 4 MiB per GPU. */
+#define SSM_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * ssm_prefill_segmented_noalloc -- ssm_prefill_segmented for callers that cannot allocate
+ * device memory when they call.  Examples are a plugin running inside a host program that
+ * owns every allocation on the GPU, and a serving loop that must not allocate once it has
+ * started, because cudaMalloc can synchronize the device and can fail under memory
+ * pressure.  The pages have no counterpart for this call: it only changes where the
+ * segment scratch lives.
+ *
+ * The scratch is a fixed array of SSM_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library holds until the process exits; nothing is allocated per call.
+ *   every argument               as for ssm_prefill_segmented, without the workspace
+ *   limit                        ssm_prefill_workspace_bytes(batch, seqlen, d_inner, seg_len)
+ *                                must not exceed SSM_NOALLOC_SCRATCH_BYTES, e.g. batch 1 with
+ *                                d_inner 8192 and 4 segments (3 MiB).  Larger requests return
+ *                                SSM_ERR_INVALID_ARG before anything runs.
+ *   first call on a device       looks up the array's device address (cudaGetSymbolAddress)
+ *                                with that device current and keeps it; make that first call
+ *                                before any stream capture.
+ *   sharing                      every call on a device uses the same array, and the array
+ *                                keeps the last call's contents.  Nothing in it needs to
+ *                                start at zero.  Calls that overlap on the GPU (other streams,
+ *                                other host threads) race on it and must be ordered by the
+ *                                caller.
+ * The result equals ssm_prefill_segmented's for the same seg_len, bit for bit.
+ */
+int ssm_prefill_segmented_noalloc(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                                  ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                  const void* x, const void* z, const void* dt,
+                                  int64_t in_stride_b, int64_t in_stride_t,
+                                  const void* Bmat, const void* Cmat,
+                                  const float* A, const float* Dskip, const float* dt_bias,
+                                  const float* conv_w, const float* conv_b,
+                                  const float* conv_state_in, const float* ssm_state_in,
+                                  int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                                  void* out, int64_t out_stride_b, int64_t out_stride_t,
+                                  float* conv_state_out, float* ssm_state_out,
+                                  int seg_len, void* cuda_stream);
+
 /*
  * ssm_decode_step -- one token per request, continuing from cached states that
  * are read and updated IN PLACE (Methodology 3: decode reuses the prefill state).

@@ -21,7 +21,9 @@ _STATUS = {0: "SSM_OK", -1: "SSM_ERR_INVALID_ARG", -2: "SSM_ERR_UNSUPPORTED", -3
 DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
 
 EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_segmented",
-           "ssm_decode_step", "ssm_decode_tokens", "q8_reduce_partials", "ssm_device_status", "ssm_last_error")
+           "ssm_prefill_segmented_noalloc", "ssm_decode_step", "ssm_decode_tokens", "q8_reduce_partials",
+           "ssm_device_status", "ssm_last_error")
+NOALLOC_SCRATCH_BYTES = 4 << 20     # SSM_NOALLOC_SCRATCH_BYTES
 
 
 class SSMError(RuntimeError):
@@ -55,6 +57,8 @@ def load(path: Path | str | None = None):
     lib.ssm_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.ssm_prefill_segmented.argtypes = lib.ssm_prefill.argtypes[:-1] + [I, P, ctypes.c_size_t, P]
     lib.ssm_prefill_segmented.restype = I
+    lib.ssm_prefill_segmented_noalloc.argtypes = lib.ssm_prefill.argtypes[:-1] + [I, P]
+    lib.ssm_prefill_segmented_noalloc.restype = I
     lib.ssm_decode_step.argtypes = [I, I, I, I, I, I, P, P, P, L, P, P, P, P, P, P, P, P, P, L, L, I, P,
                                     P, L, P]
     lib.ssm_decode_step.restype = I
@@ -141,12 +145,14 @@ def suggest_seg_len(batch: int, seqlen: int, d_inner: int, n_sm: int, ctas_per_s
 
 def prefill(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state_in=None, ssm_state_in=None,
             out=None, out_dtype=torch.float32, conv_state_out=None, ssm_state_out=None, stream=None,
-            seg_len=None, workspace=None):
+            seg_len=None, workspace=None, noalloc=False):
     """ssm_prefill over [batch, L, d_inner] x/z/dt (channel-stride-1 views allowed).
 
     With ``seg_len`` (a multiple of 64) the rows are cut into segments that run in parallel
     (ssm_prefill_segmented); ``workspace`` is then a CUDA uint8 tensor of at least
-    prefill_workspace_bytes(...) bytes, allocated here with torch when not given.
+    prefill_workspace_bytes(...) bytes, allocated here with torch when not given.  With
+    ``noalloc=True`` (and ``seg_len``) the call is ssm_prefill_segmented_noalloc: the scratch
+    is the library's fixed array of NOALLOC_SCRATCH_BYTES and no workspace is allocated.
     Returns (out, conv_state_out, ssm_state_out).
     """
     lib = load()
@@ -188,6 +194,12 @@ def prefill(x, z, dt, B, C, A, D, dt_bias, conv_w, conv_b, conv_state_in=None, s
     if seg_len is None:
         rc = lib.ssm_prefill(*args, _stream(stream))
         _check(lib, "ssm_prefill", rc)
+        return out, conv_state_out, ssm_state_out
+    if noalloc:
+        if workspace is not None:
+            raise ValueError("noalloc=True takes no workspace")
+        rc = lib.ssm_prefill_segmented_noalloc(*args, int(seg_len), _stream(stream))
+        _check(lib, "ssm_prefill_segmented_noalloc", rc)
         return out, conv_state_out, ssm_state_out
     need = int(lib.ssm_prefill_workspace_bytes(batch, L, d_inner, int(seg_len)))
     if workspace is None and need > 0:

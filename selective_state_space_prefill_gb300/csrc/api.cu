@@ -51,6 +51,36 @@ unsigned int* status_ptr(int* err) {
     return static_cast<unsigned int*>(addr);
 }
 
+}  // namespace
+
+// Scratch of ssm_prefill_segmented_noalloc: a fixed array in the library's own device
+// memory, present on every GPU that loads the library until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::atomic<void*> g_noalloc_scratch_ptr[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the array's name
+// stands for a host-side shadow, not a device address, so the address is asked of the runtime
+// (cudaGetSymbolAddress) once per device, with that device current, and cached.
+void* noalloc_scratch_ptr(int* err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = 1;
+        return nullptr;
+    }
+    void* p = g_noalloc_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+        *err = 1;
+        return nullptr;
+    }
+    g_noalloc_scratch_ptr[dev].store(addr, std::memory_order_release);
+    return addr;
+}
+
 bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool dtype_ok(int t) { return t == SSM_F32 || t == SSM_BF16; }
 int esize(int t) { return t == SSM_BF16 ? 2 : 4; }
@@ -161,7 +191,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
 
 extern "C" {
 
-int ssm_abi_version(void) { return 101; }
+int ssm_abi_version(void) { return 102; }
 
 const char* ssm_last_error(void) { return g_err; }
 
@@ -185,6 +215,40 @@ int ssm_prefill(int batch, int seqlen, int d_inner, int d_state, int d_conv,
                         in_stride_b, in_stride_t, Bmat, Cmat, A, Dskip, dt_bias, conv_w, conv_b, conv_state_in,
                         ssm_state_in, conv_state_ld, ssm_state_stride_b, out, out_stride_b, out_stride_t,
                         conv_state_out, ssm_state_out, one, nullptr, 0, cuda_stream);
+}
+
+int ssm_prefill_segmented_noalloc(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                                  ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                  const void* x, const void* z, const void* dt,
+                                  int64_t in_stride_b, int64_t in_stride_t,
+                                  const void* Bmat, const void* Cmat,
+                                  const float* A, const float* Dskip, const float* dt_bias,
+                                  const float* conv_w, const float* conv_b,
+                                  const float* conv_state_in, const float* ssm_state_in,
+                                  int64_t conv_state_ld, int64_t ssm_state_stride_b,
+                                  void* out, int64_t out_stride_b, int64_t out_stride_t,
+                                  float* conv_state_out, float* ssm_state_out,
+                                  int seg_len, void* cuda_stream) {
+    static const char* fn = "ssm_prefill_segmented_noalloc";
+    g_err[0] = 0;
+    const size_t need = ssm_prefill_workspace_bytes(batch, seqlen, d_inner, seg_len);
+    if (need > (size_t)SSM_NOALLOC_SCRATCH_BYTES)
+        return fail(SSM_ERR_INVALID_ARG,
+                    "%s: these sizes need %zu bytes of scratch and the fixed array holds %zu "
+                    "(use a longer seg_len, or ssm_prefill_segmented with a workspace)",
+                    fn, need, (size_t)SSM_NOALLOC_SCRATCH_BYTES);
+    void* ws = nullptr;
+    if (need > 0) {
+        int err = 0;
+        ws = noalloc_scratch_ptr(&err);
+        if (err) return fail(SSM_ERR_CUDA, "%s: the scratch array's device address is unavailable", fn);
+    }
+    // Nothing in the array has to start at zero: pass A writes every entry that passes B and C read.
+    return prefill_impl(fn, batch, seqlen, d_inner, d_state, d_conv, in_dtype, out_dtype, x, z, dt,
+                        in_stride_b, in_stride_t, Bmat, Cmat, A, Dskip, dt_bias, conv_w, conv_b, conv_state_in,
+                        ssm_state_in, conv_state_ld, ssm_state_stride_b, out, out_stride_b, out_stride_t,
+                        conv_state_out, ssm_state_out, seg_len, ws, (size_t)SSM_NOALLOC_SCRATCH_BYTES,
+                        cuda_stream);
 }
 
 size_t ssm_prefill_workspace_bytes(int batch, int seqlen, int d_inner, int seg_len) {
