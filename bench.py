@@ -76,9 +76,8 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_s: float) -> float
 
 # DRAM bytes (read + write) of one k_prefill launch on the bench workload, from the ncu capture
 # summarised in profiles/k_prefill_mamba130m_like_b4_l2048_d1536.md, valid only for the prefill
-# source it was taken on (first 16 hex digits of its sha256); any other source reports null.  The
-# capture predates only the removal of an unused host helper from that file; the kernel is the same.
-PREFILL_NCU_TRAFFIC = {"bytes": 76209664 + 17416448, "prefill_cu_sha256_16": "651a999a6cfcf3bc"}
+# source it was taken on (first 16 hex digits of its sha256); any other source reports null.
+PREFILL_NCU_TRAFFIC = {"bytes": 76209408 + 16988160, "prefill_cu_sha256_16": "4ec2f2a417d4917a"}
 
 
 def _prefill_traffic():
@@ -574,7 +573,8 @@ def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4, graph_calls=64):
 
 def run_profile_target(which: str):
     """Launch one kernel 4 times (3 warm-up + 1 to capture) for ncu: the prefill on the bench
-    workload, the decode step at batch 256 x d_inner 8192, or q8 over P=4 bf16 [4096, 1, 4096]."""
+    workload, the segmented prefill of a batch-1 row, the decode step at batch 256 x d_inner
+    8192, or q8 over P=4 bf16 [4096, 1, 4096]."""
     import torch
     from selective_state_space_prefill_gb300 import build as ssm_build
     if not ssm_build.up_to_date():
@@ -588,6 +588,14 @@ def run_profile_target(which: str):
         inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=torch.bfloat16, seed=0, device=dev)
         for _ in range(4):
             ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w, inp.conv_b)
+    elif which == "prefill_seg":
+        # batch-1 Falcon-Mamba-like slice (1 x 16384 x 2048) in 3 segments of 5504 tokens
+        L, D, seg = 16384, 2048, 5504
+        inp = make_mixer_inputs(1, L, D, dtype=torch.bfloat16, seed=0, device=dev)
+        ws = torch.empty(ssm.prefill_workspace_bytes(1, L, D, seg), device=dev, dtype=torch.uint8)
+        for _ in range(4):
+            ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w, inp.conv_b,
+                        seg_len=seg, workspace=ws)
     elif which == "decode":
         D, B = 8192, 256
         par = {k: v.to(dev) for k, v in make_mixer_params(D, seed=1).items()}
@@ -615,7 +623,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "decode", "q8"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8"], default=None,
                     help="only launch one kernel 4 times (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.profile:

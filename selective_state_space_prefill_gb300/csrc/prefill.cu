@@ -88,7 +88,9 @@ __device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
 }
 __device__ __forceinline__ float2 load_pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
 
-template <int S, int K, typename Tin, typename Tout>
+// kSeg: the launch covers several sequence segments (blockIdx.z); without it the CTA owns
+// the whole row and none of the segment bookkeeping is compiled in.
+template <int S, int K, typename Tin, typename Tout, bool kSeg>
 __global__ void __launch_bounds__(S * 32, 3)
 k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_B,
@@ -113,7 +115,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const bool dvalid = d < p.d_inner;
     const int L = p.seqlen;
     // sequence segment blockIdx.z: tokens [blockIdx.z * seg_len, min(L, (blockIdx.z + 1) * seg_len))
-    const int n_iter = (min(L - (int)blockIdx.z * p.seg_len, p.seg_len) + TC - 1) / TC;
+    auto seg_first_token = [&]() { return kSeg ? (int)blockIdx.z * p.seg_len : 0; };
+    const int n_iter = kSeg ? (min(L - seg_first_token(), p.seg_len) + TC - 1) / TC : (L + TC - 1) / TC;
 
     // TMA destinations need 128-byte alignment; refuse (and report) rather than fault.
     if (smem_u32(smem) & 127u) {
@@ -134,7 +137,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     auto issue = [&](int it) {
         const int s = it % kStages;
         unsigned char* st = smem + s * Lay::STAGE;
-        const int t0 = (int)blockIdx.z * p.seg_len + it * TC;
+        const int t0 = seg_first_token() + it * TC;
         mbar_arrive_expect_tx(&full[s], Lay::TX);
         tma_load_3d(st + Lay::OFF_X, &tm_x, &full[s], d0, t0 - 3, b);
         tma_load_3d(st + Lay::OFF_Z, &tm_z, &full[s], d0, t0, b);
@@ -169,7 +172,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         cb = __ldg(p.conv_b + d);
         Dd = __ldg(p.Dskip + d);
         bias = __ldg(p.dt_bias + d);
-        if (blockIdx.z > 0) {
+        if (kSeg && blockIdx.z > 0) {
             // the start state of this segment, left in the workspace by the carry pass
             const float2* hs = reinterpret_cast<const float2*>(
                 p.ws + (((int64_t)(blockIdx.z - 1) * gridDim.y + b) * p.d_inner + d) * 32 + 8 * g);
@@ -218,12 +221,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         // ---- per-token work for this lane's half of the warp's K tokens:
         //      conv + SiLU, softplus step, skip term
         const int row0 = warp * K;            // first token of this warp in the chunk
-        const int tbase = (int)blockIdx.z * p.seg_len + it * TC + row0;   // its absolute index
+        const int tbase = seg_first_token() + it * TC + row0;   // its absolute index
         const int r0 = row0 + KH * g;         // first token this lane computes
         float xm3 = to_f32(xs[(r0 + 0) * kCD + c]);   // x[t-3] (tile row 0 = chunk start - 3)
         float xm2 = to_f32(xs[(r0 + 1) * kCD + c]);
         float xm1 = to_f32(xs[(r0 + 2) * kCD + c]);
-        if (it == 0 && blockIdx.z == 0 && warp == 0 && g == 0 && p.conv_state_in != nullptr && dvalid) {
+        if (it == 0 && (!kSeg || blockIdx.z == 0) && warp == 0 && g == 0 && p.conv_state_in != nullptr && dvalid) {
             const float* cs = p.conv_state_in + (int64_t)b * 3 * p.conv_state_ld + d;
             xm3 = cs[0];
             xm2 = cs[p.conv_state_ld];
@@ -320,7 +323,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
 
     // ---- final states (last segment): h_L and the last three raw inputs
-    if ((int)blockIdx.z == p.n_seg - 1 && warp == 0 && dvalid) {
+    if ((!kSeg || (int)blockIdx.z == p.n_seg - 1) && warp == 0 && dvalid) {
         float2* hs = reinterpret_cast<float2*>(p.ssm_state_out + (int64_t)b * p.ssm_state_stride_b +
                                                (int64_t)d * kN + 8 * g);
 #pragma unroll
@@ -649,9 +652,9 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
             return -1;
         }
     }
-    static unsigned long long attr = 0;
-    auto kern = k_prefill<S, K, Tin, Tout>;
-    if (!opt_in_smem(kern, Lay::TOTAL, &attr, why)) return -1;
+    static unsigned long long attr_row = 0, attr_seg = 0;
+    auto kern = a.n_seg > 1 ? k_prefill<S, K, Tin, Tout, true> : k_prefill<S, K, Tin, Tout, false>;
+    if (!opt_in_smem(kern, Lay::TOTAL, a.n_seg > 1 ? &attr_seg : &attr_row, why)) return -1;
     kern<<<dim3(gx, q.batch, a.n_seg), S * 32, Lay::TOTAL, stream>>>(mx, mz, mdt, mB, mC, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
