@@ -511,8 +511,35 @@ def bench_decode(ssm, dev, stream, hbm_peak, steps=64, D=8192):
         gbs = decode_bytes(batch, D) / t / 1e9
         res[f"batch{batch}"] = {"steps_per_s": 1.0 / t, "us_per_step": 1e6 * t, "GB_s": gbs,
                                 "frac_hbm": gbs / hbm_peak}
-    res["note"] = ("d_inner 8192, bf16 tokens, fp32 states in place; CUDA graph of 64 back-to-back steps; "
-                   "states of batch <= 64 stay L2-resident between steps")
+    # extended sweep (the bandwidth regime): single launches, L2 flushed before each
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, device=dev)
+    for batch in (1024, 4096):
+        tok = {k: v.to(dev) for k, v in make_decode_inputs(batch, D, seed=batch).items()}
+        cs, ss = (t.to(dev) for t in make_states(batch, D, seed=batch))
+        out = torch.empty(batch, D, device=dev)
+        f = lambda: ssm.decode_step(tok["x"], tok["z"], tok["dt"], tok["B"], tok["C"], par["A"], par["D"],
+                                    par["dt_bias"], par["conv_w"], par["conv_b"], cs, ss, out=out, stream=stream)
+        for _ in range(3):
+            f()
+        ts = []
+        for k in range(5):
+            flush.fill_(float(k))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        t = statistics.median(a.elapsed_time(b) for a, b in ts) / 1e3
+        gbs = decode_bytes(batch, D) / t / 1e9
+        res[f"batch{batch}"] = {"steps_per_s": 1.0 / t, "us_per_step": 1e6 * t, "GB_s": gbs, "frac_hbm": gbs / hbm_peak,
+                                "timing": "extended size: single launch, L2 flushed before it"}
+        del tok, cs, ss, out
+    del flush
+    torch.cuda.empty_cache()
+    res["note"] = ("d_inner 8192, bf16 tokens, fp32 states in place; batch <= 256: CUDA graph of 64 back-to-back "
+                   "steps, states of batch <= 64 stay L2-resident between steps; batch 1024/4096: extended sizes")
     return res
 
 
@@ -520,7 +547,7 @@ def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4, graph_calls=64):
     import torch
     from selective_state_space_prefill_gb300.inputs import make_partials
     res = {}
-    for batch in (1, 8, 64, 256, 4096):
+    for batch in (1, 8, 64, 256, 4096, 16384):
         n = batch * 4096
         parts = [p.to(dev) for p in make_partials(P, (batch, 1, 4096), dtype=torch.bfloat16, seed=batch)]
         out = torch.empty(batch, 1, 4096, device=dev, dtype=torch.bfloat16)
@@ -567,7 +594,8 @@ def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4, graph_calls=64):
                                 "timing": "single launch, L2 flushed before it"}
     res["note"] = ("P=4 bf16 partials [batch,1,4096], block 128, bf16 out + int32 sums + scales; "
                    "batch <= 256: CUDA graph of back-to-back calls with L2-resident operands, so GB_s there "
-                   "is not an HBM figure; batch 4096 is an extended size showing the bandwidth regime")
+                   "is not an HBM figure; batch 4096 and 16384 (2^26 elements) are extended sizes showing the "
+                   "bandwidth regime")
     return res
 
 
