@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the selective-SSM mixer (test infrastructure only).
+"""fp64 CPU oracle for the selective-SSM mixer and its output-projection partial
+(test infrastructure only).
 
 Only the test-suite, the smoke check and the benchmark's CPU-baseline leg may
 import this package.  It shares no code with the CUDA path: the arithmetic
@@ -13,6 +14,7 @@ from .oracle import (  # noqa: F401
     build,
     decode_step,
     lib_path,
+    out_proj,
     prefill,
     q8_reduce,
     scan_chunked,

@@ -56,6 +56,8 @@ def _bind(lib):
     lib.oracle_scan_chunked.restype = None
     lib.oracle_q8_reduce.argtypes = [I, P, I, L, I, P, P, P, P]
     lib.oracle_q8_reduce.restype = I
+    lib.oracle_out_proj.argtypes = [L, L, L, I, P, P, P, P, P, I]
+    lib.oracle_out_proj.restype = I
     return lib
 
 
@@ -227,3 +229,29 @@ def q8_reduce(partials, block=128, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_q8_reduce rejected the sizes (rc={rc})")
     return dict(sums=sums, scales=scales, out_f32=out_f32, out_bf16=out_bf16)
+
+
+def out_proj(y, W, n_threads=None, lib=None):
+    """One rank's out_proj partial: y [M, K] and W [N, K] (same dtype).
+
+    Returns dict(out [M, N] float64, amax [ceil(M*N/128)] float64, absdot [M, N] float64),
+    absdot = |y| @ |W|^T (the scale of the rounding error of any fp32 evaluation).
+    """
+    lib = lib or load()
+    yr, cy = _raw(y)
+    wr, cw = _raw(W)
+    if cy != cw:
+        raise TypeError("y and W must share one dtype")
+    yr = np.ascontiguousarray(yr.reshape(yr.shape[0], -1) if yr.ndim > 2 else yr)
+    wr = np.ascontiguousarray(wr)
+    M, K = yr.shape
+    N, K2 = wr.shape
+    if K != K2:
+        raise ValueError("y and W disagree on K")
+    out = np.empty((M, N), np.float64)
+    absdot = np.empty((M, N), np.float64)
+    amax = np.empty(((M * N) + 127) // 128, np.float64)
+    rc = lib.oracle_out_proj(M, N, K, cy, _p(yr), _p(wr), _p(out), _p(amax), _p(absdot), _threads(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_out_proj rejected its arguments")
+    return dict(out=out, amax=amax, absdot=absdot)

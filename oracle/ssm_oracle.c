@@ -297,3 +297,56 @@ int oracle_q8_reduce(int P, const void* const* partials, int in_dtype, int64_t n
     }
     return 0;
 }
+
+/*
+ * oracle_out_proj -- one tensor-parallel rank's partial of the mixer's output
+ * projection, the operand of the quantized all-reduce ("Scaling State-Space
+ * Models on Multiple GPUs with Tensor Parallelism", Methodology 1: the layer is
+ * split along the feature dimension; Methodology 4: the ranks' partial outputs
+ * are quantized, summed and dequantized).  The rank holds the mixer output of
+ * its channel slice, y [M][K] (M = batch * tokens, K = channels of the slice),
+ * and the matching columns of the projection weight, W [N][K] (N = model width).
+ * Its partial is
+ *   out[m][n] = sum_k y[m][k] * W[n][k]                          (double, k in order)
+ * and, for the shared-scale codec, the absolute maximum of every block of 128
+ * consecutive elements of the row-major [M][N] partial (the last block may be
+ * shorter):
+ *   amax[j] = max_{i in block j} |out_i|.
+ * absdot[m][n] = sum_k |y[m][k]| * |W[n][k]| (nullable) bounds the rounding of
+ * any fp32 evaluation of the same sum.
+ *   y, W      in_dtype elements, row-major, contiguous
+ *   out       [M][N] double;  amax  [ceil(M*N/128)] double (nullable)
+ */
+int oracle_out_proj(int64_t M, int64_t N, int64_t K, int in_dtype, const void* y, const void* W,
+                    double* out, double* amax, double* absdot, int n_threads)
+{
+    if (M < 1 || N < 1 || K < 1) return -1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0, a = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double yv = widen(y, in_dtype, m * K + k);
+                const double wv = widen(W, in_dtype, n * K + k);
+                s += yv * wv;
+                a += fabs(yv) * fabs(wv);
+            }
+            out[m * N + n] = s;
+            if (absdot) absdot[m * N + n] = a;
+        }
+    }
+    if (amax) {
+        const int64_t total = M * N;
+        for (int64_t j0 = 0; j0 < total; j0 += 128) {
+            const int64_t j1 = j0 + 128 < total ? j0 + 128 : total;
+            double mx = 0.0;
+            for (int64_t i = j0; i < j1; ++i)
+                if (fabs(out[i]) > mx) mx = fabs(out[i]);
+            amax[j0 / 128] = mx;
+        }
+    }
+    return 0;
+}

@@ -132,3 +132,13 @@ def make_partials(P: int, shape, dtype=torch.bfloat16, seed: int = 0, device="cp
     g = _gen(seed + 32452843, device)
     return [torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dtype)
             for _ in range(P)]
+
+
+def make_out_proj_inputs(M: int, K: int, N: int, dtype=torch.bfloat16, seed: int = 0,
+                         device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+    """One rank's out_proj operands: the mixer output of its channel slice y [M, K] ~ N(0, 1)
+    and the matching weight columns W [N, K] ~ N(0, 1/K) (the usual fan-in scale)."""
+    g = _gen(seed + 15485863, device)
+    y = torch.randn(M, K, generator=g, device=device, dtype=torch.float32).to(dtype)
+    W = (torch.randn(N, K, generator=g, device=device, dtype=torch.float32) / K ** 0.5).to(dtype)
+    return y, W

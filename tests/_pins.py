@@ -10,7 +10,9 @@ copy) and raises AssertionError when the oracle disagrees with:
 * the state-caching invariant (prefill then decode = longer prefill) and channel-
   slice independence from the pages' Methodology 2 and 3,
 * hand-derived cases of the 8-bit reduction (tests/golden/q8_hand_cases.txt) and
-  its per-block error bound.
+  its per-block error bound,
+* an independent fp64 matrix product and closed forms (identity, rank one) for the
+  output-projection partial.
 
 The same pins run against deliberately broken copies of the oracle source in
 ``test_oracle_mutations.py``; each planted mistake must fail at least one pin.
@@ -325,9 +327,43 @@ def pin_q8_bounds(lib, P=4, n=4096 + 77, block=128):
     assert np.array_equal(r["out_bf16"], bf), "bf16 rounding of the output"
 
 
+
+def pin_out_proj_vs_matmul(lib):
+    """The partial equals an independent fp64 matrix product of the widened inputs; absdot is
+    |y| |W|^T; the block maxima are those of the row-major partial, the last block short."""
+    g = torch.Generator().manual_seed(7)
+    for dtype in (torch.bfloat16, torch.float32):
+        y = torch.randn(33, 70, generator=g).to(dtype)
+        W = torch.randn(21, 70, generator=g).to(dtype)
+        r = orc.out_proj(y, W, lib=lib)
+        yd, wd = _np64(y), _np64(W)
+        ref = yd @ wd.T
+        _close(r["out"], ref, 1e-12, "out_proj vs matmul")
+        _close(r["absdot"], np.abs(yd) @ np.abs(wd).T, 1e-12, "absdot")
+        flat = np.abs(ref).reshape(-1)
+        blocks = [flat[i:i + 128].max() for i in range(0, flat.size, 128)]
+        assert r["amax"].shape == (len(blocks),) and flat.size % 128 != 0
+        _close(r["amax"], np.array(blocks), 1e-12, "block amax")
+
+
+def pin_out_proj_identity_and_rank_one(lib):
+    """W = I returns y exactly; rank-one y and W give the closed form u_m p_n (v . q)."""
+    y = torch.randn(9, 16, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    r = orc.out_proj(y, torch.eye(16).to(torch.bfloat16), lib=lib)
+    assert np.array_equal(r["out"], _np64(y)), "identity"
+    u = np.array([1, -2, 3, 0.5, -4], np.float64)
+    v = np.array([2, -1, 0.25, 3, 1, -2, 0.5], np.float64)
+    pn = np.array([-1, 2, 0.5], np.float64)
+    q = np.array([1, 1, -3, 0.5, 2, -1, 4], np.float64)
+    yy = torch.from_numpy(np.outer(u, v)).to(torch.bfloat16)   # small dyadic values: exact in bf16
+    WW = torch.from_numpy(np.outer(pn, q)).to(torch.bfloat16)
+    r = orc.out_proj(yy, WW, lib=lib)
+    assert np.array_equal(r["out"], np.outer(u, pn) * float(v @ q)), "rank one"
+
 MIXER_PINS = [pin_brute_force, pin_brute_force_bf16, pin_short_sequence, pin_prefix_sum_A_zero,
               pin_geometric_series, pin_C_zero_skip_gate, pin_softplus_ln2, pin_state_caching,
               pin_decode_matches_brute, pin_split_invariance]
 SCAN_PINS = [pin_scan_sequential, pin_scan_chunked]
 Q8_PINS = [pin_q8_hand_cases, pin_q8_bounds]
-ALL_PINS = MIXER_PINS + SCAN_PINS + Q8_PINS
+OUT_PROJ_PINS = [pin_out_proj_vs_matmul, pin_out_proj_identity_and_rank_one]
+ALL_PINS = MIXER_PINS + SCAN_PINS + Q8_PINS + OUT_PROJ_PINS

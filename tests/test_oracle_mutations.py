@@ -44,6 +44,12 @@ MUTATIONS = {
     "q8_per_partial_amax": ("for (int p = 0; p < P; ++p)\n            for (int64_t i = j0; i < j1; ++i) {",
                             "for (int p = 0; p < 1; ++p)\n            for (int64_t i = j0; i < j1; ++i) {"),
     "q8_output_scale": ("float o = (float)s * scale;", "float o = (float)s * inv;"),
+    "out_proj_W_transposed": ("const double wv = widen(W, in_dtype, n * K + k);",
+                              "const double wv = widen(W, in_dtype, k * N + n);"),
+    "out_proj_drops_last_k": ("for (int64_t k = 0; k < K; ++k) {\n                const double yv",
+                              "for (int64_t k = 0; k < K - 1; ++k) {\n                const double yv"),
+    "out_proj_absdot_signed": ("a += fabs(yv) * fabs(wv);", "a += yv * wv;"),
+    "out_proj_amax_signed": ("if (fabs(out[i]) > mx) mx = fabs(out[i]);", "if (out[i] > mx) mx = out[i];"),
 }
 
 
