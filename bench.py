@@ -167,6 +167,14 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _tc_peak():
+    """Measured dense bf16 tensor TFLOP/s (burst) from MEASURED_PEAKS.json, else the fallback 1900."""
+    try:
+        return float(json.loads((ROOT / "MEASURED_PEAKS.json").read_text())["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def _cpu_oracle_run(inp, budget_s, threads):
     """Run the fp64 oracle over the whole workload until `budget_s` has elapsed (at least once)."""
     import oracle
@@ -309,6 +317,7 @@ def run_ours(args):
         extras["q8"] = bench_q8(ssm, dev, stream, hbm_peak, flush)
         extras["prefill_other_workloads"] = bench_prefill_other(ssm, dev, stream, hbm_peak, flush)
         extras["decode_block"] = bench_decode_block(ssm, dev, stream, hbm_peak, flush)
+        extras["out_proj"] = bench_out_proj(ssm, dev, stream, flush, _tc_peak())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -444,6 +453,47 @@ def bench_prefill_other(ssm, dev, stream, hbm_peak, flush):
                                  "kernels": "k_prefill_agg + k_prefill_carry + k_prefill"})
         del inp, out, ws
         torch.cuda.empty_cache()
+    return res
+
+
+def bench_out_proj(ssm, dev, stream, flush, tc_peak):
+    """One rank's out_proj partial on the tensor cores (bf16 in, fp32 accumulate, bf16 out plus
+    per-128-block maxima): TFLOP/s against the measured bf16 tensor peak, L2 flushed before each
+    of 10 timed launches.  cuBLAS (torch.matmul, bf16) on the same operands is timed as context."""
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_out_proj_inputs
+    res = {}
+    for name, (M, N, K) in {"falcon_mamba7b_like_rank_M16384_N4096_K2048": (16384, 4096, 2048),
+                            "mamba130m_like_layer_M8192_N768_K1536": (8192, 768, 1536)}.items():
+        y, W = make_out_proj_inputs(M, K, N, seed=0, device=dev)
+        out = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        amax = torch.empty(M * N // 128, device=dev)
+        times = {}
+        for impl in ("ours", "cublas"):
+            if impl == "ours":
+                f = lambda: ssm.out_proj_partial(y, W, out=out, block_amax=amax, stream=stream)
+            else:
+                f = lambda: torch.matmul(y, W.t(), out=out)
+            for _ in range(3):
+                f()
+            ts = []
+            for k in range(10):
+                flush.fill_(float(k))
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                f()
+                b_.record(stream)
+                ts.append((a, b_))
+            torch.cuda.synchronize(dev)
+            times[impl] = statistics.median(a.elapsed_time(b_) for a, b_ in ts) / 1e3
+        flops = 2.0 * M * N * K
+        t = times["ours"]
+        res[name] = {"us": 1e6 * t, "TFLOP_s": flops / t / 1e12, "frac_tensor": flops / t / 1e12 / tc_peak,
+                     "cublas_us": 1e6 * times["cublas"], "cublas_TFLOP_s": flops / times["cublas"] / 1e12}
+        del y, W, out, amax
+        torch.cuda.empty_cache()
+    res["note"] = ("k_out_proj: tcgen05.mma kind::f16, 128x256 tiles, 4-stage TMA ring, TMEM accumulator; "
+                   "frac_tensor against MEASURED_PEAKS.json bf16_tflops (burst); cuBLAS is context, not used")
     return res
 
 
@@ -602,7 +652,8 @@ def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4, graph_calls=64):
 def run_profile_target(which: str):
     """Launch one kernel 4 times (3 warm-up + 1 to capture) for ncu: the prefill on the bench
     workload, the segmented prefill of a batch-1 row, the decode step at batch 256 x d_inner
-    8192, or q8 over P=4 bf16 [4096, 1, 4096]."""
+    8192, q8 over P=4 bf16 [4096, 1, 4096], or the out_proj partial of the Falcon-Mamba-like
+    rank (16384 x 4096 x 2048)."""
     import torch
     from selective_state_space_prefill_gb300 import build as ssm_build
     if not ssm_build.up_to_date():
@@ -633,6 +684,11 @@ def run_profile_target(which: str):
         for _ in range(4):
             ssm.decode_step(tok["x"], tok["z"], tok["dt"], tok["B"], tok["C"], par["A"], par["D"],
                             par["dt_bias"], par["conv_w"], par["conv_b"], cs, ss, out=out)
+    elif which == "out_proj":
+        from selective_state_space_prefill_gb300.inputs import make_out_proj_inputs
+        y, W = make_out_proj_inputs(16384, 2048, 4096, seed=0, device=dev)
+        for _ in range(4):
+            ssm.out_proj_partial(y, W)
     else:
         parts = [q.to(dev) for q in make_partials(4, (4096, 1, 4096), dtype=torch.bfloat16, seed=4096)]
         for _ in range(4):
@@ -651,7 +707,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8", "out_proj"], default=None,
                     help="only launch one kernel 4 times (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.profile:

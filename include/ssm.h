@@ -261,6 +261,31 @@ int ssm_decode_tokens(int batch, int n_tokens, int d_inner, int d_state, int d_c
                       void* cuda_stream);
 
 /*
+ * ssm_out_proj_partial -- one tensor-parallel rank's partial of the mixer's output
+ * projection, on the tensor cores.  Methodology 1 splits the layer along the feature
+ * dimension, so a rank holds the mixer output of its channel slice and the matching
+ * columns of the projection weight.  Methodology 4 sums the ranks' partials through the
+ * 8-bit all-reduce.
+ *   out[m][n] = sum_k y[m][k] * W[n][k]     (bf16 products, fp32 accumulation)
+ * When block_amax is not NULL: block_amax[j] = max |out_i| over block j of 128 consecutive
+ * elements of the row-major [M][N] partial.  The maximum is taken over the values stored in
+ * `out`, so it equals what q8_reduce_partials would find in them.  The all-reduce's
+ * shared scale is the maximum of the ranks' block_amax.
+ *
+ *   M, N, K                  rows (batch x tokens), model width, channels of the slice;
+ *                            N % 128 == 0, K % 8 == 0, M <= 65535 * 128
+ *   y, ldy                   [M][K] bf16, row stride ldy >= K (a multiple of 8), 16-byte aligned
+ *   W, ldw                   [N][K] bf16: the weight's columns for the slice, K contiguous
+ *   out_dtype, out, ldo      [M][N] SSM_BF16 (round to nearest even) or SSM_F32, row
+ *                            stride ldo >= N (a multiple of 8), 16-byte aligned
+ *   block_amax               NULL or [M * N / 128] float32
+ * Returns SSM_OK or a negative status.
+ */
+int ssm_out_proj_partial(int64_t M, int64_t N, int64_t K, const void* y, int64_t ldy,
+                         const void* W, int64_t ldw, ssm_dtype_t out_dtype, void* out, int64_t ldo,
+                         float* block_amax, void* cuda_stream);
+
+/*
  * q8_reduce_partials -- the arithmetic of the pages' 8-bit quantized all-reduce
  * (Methodology 4), done locally over P partial buffers already in this GPU's
  * memory: quantize every partial to int8 with one scale per block of `block`

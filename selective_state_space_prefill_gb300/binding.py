@@ -21,8 +21,8 @@ _STATUS = {0: "SSM_OK", -1: "SSM_ERR_INVALID_ARG", -2: "SSM_ERR_UNSUPPORTED", -3
 DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
 
 EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_segmented",
-           "ssm_prefill_segmented_noalloc", "ssm_decode_step", "ssm_decode_tokens", "q8_reduce_partials",
-           "ssm_device_status", "ssm_last_error")
+           "ssm_prefill_segmented_noalloc", "ssm_decode_step", "ssm_decode_tokens", "ssm_out_proj_partial",
+           "q8_reduce_partials", "ssm_device_status", "ssm_last_error")
 NOALLOC_SCRATCH_BYTES = 4 << 20     # SSM_NOALLOC_SCRATCH_BYTES
 
 
@@ -65,6 +65,8 @@ def load(path: Path | str | None = None):
     lib.ssm_decode_tokens.argtypes = [I, I, I, I, I, I, I, P, P, P, L, L, P, P, P, P, P, P, P, P, P, L, L, I,
                                       P, P, L, L, P]
     lib.ssm_decode_tokens.restype = I
+    lib.ssm_out_proj_partial.argtypes = [L, L, L, P, L, P, L, I, P, L, P, P]
+    lib.ssm_out_proj_partial.restype = I
     lib.q8_reduce_partials.argtypes = [I, P, I, L, I, P, I, P, P, P]
     lib.q8_reduce_partials.restype = I
     lib.ssm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
@@ -327,3 +329,31 @@ def device_status(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check(lib, "ssm_device_status", lib.ssm_device_status(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+def out_proj_partial(y, W, out=None, out_dtype=torch.bfloat16, block_amax=True, stream=None):
+    """ssm_out_proj_partial: y [M, K] bf16 and W [N, K] bf16 (row views with stride-1 K).
+
+    Returns (out [M, N], block_amax [M*N/128] float32 or None).
+    """
+    lib = load()
+    _need_cuda(y, W, out)
+    if y.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("y and W must be bfloat16")
+    if y.dim() != 2 or W.dim() != 2 or y.stride(1) != 1 or W.stride(1) != 1 or y.shape[1] != W.shape[1]:
+        raise ValueError("y [M, K] and W [N, K] must be 2-D with a stride-1 K dimension")
+    M, K = y.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty(M, N, device=y.device, dtype=out_dtype)
+    if out.dim() != 2 or tuple(out.shape) != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with a stride-1 N dimension")
+    amax = None
+    if block_amax is True:
+        amax = torch.empty((M * N + 127) // 128, device=y.device, dtype=torch.float32)
+    elif block_amax is not None and block_amax is not False:
+        amax = block_amax
+    rc = lib.ssm_out_proj_partial(M, N, K, _ptr(y), y.stride(0), _ptr(W), W.stride(0), _dtype_code(out.dtype),
+                                  _ptr(out), out.stride(0), _ptr(amax), _stream(stream))
+    _check(lib, "ssm_out_proj_partial", rc)
+    return out, amax

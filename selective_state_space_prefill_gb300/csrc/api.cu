@@ -191,7 +191,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
 
 extern "C" {
 
-int ssm_abi_version(void) { return 102; }
+int ssm_abi_version(void) { return 103; }
 
 const char* ssm_last_error(void) { return g_err; }
 
@@ -249,6 +249,40 @@ int ssm_prefill_segmented_noalloc(int batch, int seqlen, int d_inner, int d_stat
                         ssm_state_in, conv_state_ld, ssm_state_stride_b, out, out_stride_b, out_stride_t,
                         conv_state_out, ssm_state_out, seg_len, ws, (size_t)SSM_NOALLOC_SCRATCH_BYTES,
                         cuda_stream);
+}
+
+int ssm_out_proj_partial(int64_t M, int64_t N, int64_t K, const void* y, int64_t ldy, const void* W, int64_t ldw,
+                         ssm_dtype_t out_dtype, void* out, int64_t ldo, float* block_amax, void* cuda_stream) {
+    static const char* fn = "ssm_out_proj_partial";
+    g_err[0] = 0;
+    if (M < 1 || M > 65535LL * 128) return fail(SSM_ERR_INVALID_ARG, "%s: M %lld not in [1, 65535*128]", fn, (long long)M);
+    if (N < 1 || N > 65535LL * 256) return fail(SSM_ERR_INVALID_ARG, "%s: N %lld not in [1, 65535*256]", fn, (long long)N);
+    if (K < 1 || K > (1LL << 31)) return fail(SSM_ERR_INVALID_ARG, "%s: K %lld out of range", fn, (long long)K);
+    if (!dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (!y || !W || !out) return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (N % 128 != 0) return fail(SSM_ERR_UNSUPPORTED, "%s: N %lld is not a multiple of 128", fn, (long long)N);
+    if (K % 8 != 0) return fail(SSM_ERR_UNSUPPORTED, "%s: K %lld is not a multiple of 8", fn, (long long)K);
+    if (ldy < K || ldw < K || ldo < N) return fail(SSM_ERR_INVALID_ARG, "%s: a row stride is below the row length", fn);
+    if (ldy % 8 != 0 || ldw % 8 != 0 || ldo % 8 != 0)
+        return fail(SSM_ERR_MISALIGNED, "%s: row strides must be multiples of 8 elements", fn);
+    if (!aligned(y, 16) || !aligned(W, 16) || !aligned(out, 16) || (block_amax && !aligned(block_amax, 4)))
+        return fail(SSM_ERR_MISALIGNED, "%s: y, W and out must be 16-byte aligned", fn);
+
+    int serr = 0;
+    unsigned int* status = status_ptr(&serr);
+    if (serr) return fail(SSM_ERR_CUDA, "%s: no usable CUDA device", fn);
+    ssm::OutProjArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.out = out;
+    a.ldo = ldo;
+    a.amax = block_amax;
+    a.status = status;
+    const char* why = "";
+    if (ssm::launch_out_proj(a, y, W, ldy, ldw, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
+    return SSM_OK;
 }
 
 size_t ssm_prefill_workspace_bytes(int batch, int seqlen, int d_inner, int seg_len) {

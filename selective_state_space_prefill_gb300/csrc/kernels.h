@@ -62,9 +62,21 @@ struct Q8Args {
     float* scales;
 };
 
+// Output projection partial: out [M][N] (row stride ldo) = y [M][K] W[N][K]^T, and
+// amax[j] = max |out| over the 128-element block j of the row-major [M][N] partial.
+struct OutProjArgs {
+    int64_t M, N, K;
+    void* out;
+    int64_t ldo;
+    float* amax;
+    unsigned int* status;
+};
+
 // Each returns 0 on success, or -1 with *why set to a static message.
 int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why);
 int launch_decode(const DecodeArgs& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
 int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
+int launch_out_proj(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, int64_t ldw, bool out_bf16,
+                    cudaStream_t stream, const char** why);
 
 }  // namespace ssm

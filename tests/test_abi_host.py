@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding.EXPORTS)
     for fn in names:
         assert hasattr(lib, fn), fn
-    assert lib.ssm_abi_version() == 102
+    assert lib.ssm_abi_version() == 103
 
 
 FAKE = 0x10000  # 64 KiB-aligned fake device address, never dereferenced
@@ -173,3 +173,21 @@ def test_suggest_seg_len():
     assert binding.suggest_seg_len(1, 16384, 2048, 152) == 5504          # 3 segments
     assert binding.suggest_seg_len(1, 100, 64, 152) == 64
     assert binding.suggest_seg_len(1, 64, 64, 152) is None               # a single chunk
+
+
+def _out_proj(lib, **kw):
+    a = dict(M=256, N=768, K=1536, y=FAKE, ldy=1536, W=FAKE, ldw=1536, out_dtype=1, out=FAKE, ldo=768,
+             amax=None, stream=None)
+    a.update(kw)
+    return lib.ssm_out_proj_partial(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=0), INVALID), (dict(N=0), INVALID), (dict(K=0), INVALID), (dict(out_dtype=5), INVALID),
+    (dict(y=None), INVALID), (dict(N=700, ldo=704), UNSUPPORTED), (dict(K=1540, ldy=1544, ldw=1544), UNSUPPORTED),
+    (dict(ldy=1024), INVALID), (dict(ldo=700), INVALID), (dict(ldw=1540), MISALIGNED),
+    (dict(y=FAKE + 8), MISALIGNED), (dict(out=FAKE + 4), MISALIGNED), (dict(M=65535 * 128 + 1), INVALID),
+])
+def test_out_proj_rejects_bad_arguments(lib, kw, code):
+    assert _out_proj(lib, **kw) == code
+    assert lib.ssm_last_error().decode().startswith("ssm_out_proj_partial")
