@@ -32,15 +32,25 @@
 namespace ssm {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kStages = 4;
+constexpr int kBM = 128, kBK = 64;
 constexpr int kThreads = 192;                       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kABytes = kBM * kBK * 2;              // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;              // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;      // 48 KB, a multiple of 1024
-constexpr int kOffBar = kStages * kStageBytes;      // full[S], empty[S], acc_full[2], acc_empty[2], TMEM address
-constexpr int kSmemBytes = kOffBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + slack to align to 1024
-constexpr uint32_t kTmemCols = 2 * kBN;             // two fp32 accumulators of 128 lanes x 256 columns
+
+// Tile geometry for an output tile of 128 x BN (BN = 256, or 128 for problems with few tiles).
+template <int BN>
+struct Geo {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;    // a multiple of 1024
+    static constexpr int kOffBar = kStages * kStageBytes;    // full[S], empty[S], acc_full[2], acc_empty[2], TMEM address
+    static constexpr int kSmemBytes = kOffBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + slack to align to 1024
+    static constexpr uint32_t kTmemCols = 2 * BN;            // two fp32 accumulators of 128 lanes x BN columns
+    // tcgen05.mma kind::f16 instruction descriptor: fp32 accumulator (bits 4-5 = 1), bf16 A and B
+    // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+    // M >> 4 at bits 24-28.
+    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                       ((uint32_t)(kBM >> 4) << 24);
+};
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with 128-byte swizzling:
 // rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked along M/N.
@@ -58,12 +68,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A and
-// B (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kBM >> 4) << 24);
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -72,12 +76,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
         : "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -107,10 +112,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <typename Tout>
+template <typename Tout, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
 k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
            const OutProjArgs p) {
+    using G = Geo<kBN>;
+    constexpr int kStages = G::kStages, kStageBytes = G::kStageBytes, kOffBar = G::kOffBar;
+    constexpr uint32_t kTmemCols = G::kTmemCols;
     extern __shared__ unsigned char smem_raw[];
     // TMA 128-byte swizzling and the descriptors' base offset 0 want 1024-byte aligned tiles
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -194,7 +202,8 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
                 const uint32_t b0 = a0 + kABytes;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)      // 16 bf16 = 32 bytes along K per MMA
-                    mma_bf16(dt, smem_desc_sw128(a0 + 32 * kk), smem_desc_sw128(b0 + 32 * kk), (kb | kk) != 0);
+                    mma_bf16(dt, smem_desc_sw128(a0 + 32 * kk), smem_desc_sw128(b0 + 32 * kk), G::kIdesc,
+                             (kb | kk) != 0);
                 mma_commit(&empty[s]);                      // the stage is free once these MMAs are done
             }
             mma_commit(&acc_full[buf]);                     // the tile is complete in buffer buf
@@ -287,48 +296,57 @@ bool make_map_kmajor(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-int launch_out_proj(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, int64_t ldw, bool out_bf16,
-                    cudaStream_t stream, const char** why) {
+template <typename Tout, int BN>
+int launch_bn(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, int64_t ldw, int dev, int n_sm,
+              cudaStream_t stream, const char** why) {
+    using G = Geo<BN>;
     CUtensorMap ma, mb;
     if (!make_map_kmajor(&ma, y, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)ldy, kBM) ||
-        !make_map_kmajor(&mb, W, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)ldw, kBN)) {
+        !make_map_kmajor(&mb, W, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)ldw, BN)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
         return -1;
     }
-    auto kern = out_bf16 ? k_out_proj<__nv_bfloat16> : k_out_proj<float>;
-    static unsigned long long done_bf16 = 0, done_f32 = 0;
-    unsigned long long* done = out_bf16 ? &done_bf16 : &done_f32;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        *why = "cudaGetDevice failed";
-        return -1;
-    }
+    auto kern = k_out_proj<Tout, BN>;
+    static unsigned long long done = 0;
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
+    if (!(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) != cudaSuccess) {
             *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
             return -1;
         }
-        __atomic_fetch_or(done, bit, __ATOMIC_ACQ_REL);
+        __atomic_fetch_or(&done, bit, __ATOMIC_ACQ_REL);
     }
-    // persistent: one CTA per SM (the 196 KB of shared memory allow no second one, which also
-    // leaves the SM's 512 TMEM columns to this CTA), looping over the output tiles
-    int n_sm = 0;
-    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
-        *why = "cudaDeviceGetAttribute(MultiProcessorCount) failed";
-        return -1;
-    }
-    const int64_t tiles = ((a.N + kBN - 1) / kBN) * ((a.M + kBM - 1) / kBM);
+    // persistent: one CTA per SM (the shared memory allows no second one, which also leaves the
+    // SM's TMEM columns to this CTA), looping over the output tiles
+    const int64_t tiles = ((a.N + BN - 1) / BN) * ((a.M + kBM - 1) / kBM);
     const dim3 grid((unsigned)(tiles < n_sm ? tiles : n_sm));
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, a);
+    kern<<<grid, kThreads, G::kSmemBytes, stream>>>(ma, mb, a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return -1;
     }
     return 0;
+}
+
+}  // namespace
+
+int launch_out_proj(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, int64_t ldw, bool out_bf16,
+                    cudaStream_t stream, const char** why) {
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
+        *why = "cudaGetDevice / multiprocessor count failed";
+        return -1;
+    }
+    // 256-column tiles unless that leaves fewer than two tiles per SM; then 128 columns
+    const int64_t tiles256 = ((a.N + 255) / 256) * ((a.M + kBM - 1) / kBM);
+    const bool narrow = tiles256 < 2 * (int64_t)n_sm;
+    if (out_bf16)
+        return narrow ? launch_bn<__nv_bfloat16, 128>(a, y, W, ldy, ldw, dev, n_sm, stream, why)
+                      : launch_bn<__nv_bfloat16, 256>(a, y, W, ldy, ldw, dev, n_sm, stream, why);
+    return narrow ? launch_bn<float, 128>(a, y, W, ldy, ldw, dev, n_sm, stream, why)
+                  : launch_bn<float, 256>(a, y, W, ldy, ldw, dev, n_sm, stream, why);
 }
 
 }  // namespace ssm

@@ -87,3 +87,17 @@ def test_out_proj_falcon_slice_sampled_and_q8():
     shared = torch.maximum(amax, amax2).cpu().numpy()
     expect = np.where(shared > 0, shared / np.float32(127.0), np.float32(0.0)).astype(np.float32)   # IEEE fp32 division
     assert np.array_equal(scales.cpu().numpy(), expect)
+
+
+def test_out_proj_wide_tiles_ragged():
+    """Enough tiles for the 256-column path, with a ragged M, a half-filled last N tile and a
+    ragged K; sampled rows against the oracle, block maxima against the stored partial."""
+    M, N, K = 128 * 152 + 77, 640, 200
+    y, W = make_out_proj_inputs(M, K, N, seed=11, device=DEV)
+    for out_dtype in (torch.bfloat16, torch.float32):
+        out, amax = ssm.out_proj_partial(y, W, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        rows = np.array([0, 129, 9000, M - 78, M - 77, M - 1])
+        ref = oracle.out_proj(y[torch.as_tensor(rows, device=DEV)].cpu(), W.cpu())
+        _check(y, W, out, None, ref, out_dtype, rows=rows)
+        assert torch.equal(amax, out.float().abs().reshape(-1, 128).amax(1))
