@@ -318,6 +318,7 @@ def run_ours(args):
         extras["prefill_other_workloads"] = bench_prefill_other(ssm, dev, stream, hbm_peak, flush)
         extras["decode_block"] = bench_decode_block(ssm, dev, stream, hbm_peak, flush)
         extras["out_proj"] = bench_out_proj(ssm, dev, stream, flush, _tc_peak())
+        extras["decode_configs"] = bench_decode_configs(ssm, dev, stream, hbm_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -328,6 +329,15 @@ def run_ours(args):
         reps, el = _cpu_oracle_run(cpu_inp, args.cpu_seconds, threads)
         cpu = {"value": reps * B * L / el, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"the whole workload (all {D} channels x {B} x {L} tokens), {reps} run(s) in {el:.1f} s"}
+        # one host thread on a channel sample (channels are independent, so the rate scales)
+        import oracle as _orc
+        n1 = 96
+        t1 = time.perf_counter()
+        _orc.prefill(cpu_inp.x, cpu_inp.z, cpu_inp.dt, cpu_inp.B, cpu_inp.C, cpu_inp.A, cpu_inp.D, cpu_inp.dt_bias,
+                     cpu_inp.conv_w, cpu_inp.conv_b, channels=list(range(n1)), n_threads=1)
+        t1 = time.perf_counter() - t1
+        cpu["one_thread_value"] = B * L * n1 / D / t1
+        cpu["one_thread_sample"] = f"{n1} of {D} channels x {B} x {L} tokens on 1 thread in {t1:.2f} s"
 
     if rank == 0:
         line = {
@@ -590,6 +600,48 @@ def bench_decode(ssm, dev, stream, hbm_peak, steps=64, D=8192):
     torch.cuda.empty_cache()
     res["note"] = ("d_inner 8192, bf16 tokens, fp32 states in place; batch <= 256: CUDA graph of 64 back-to-back "
                    "steps, states of batch <= 64 stay L2-resident between steps; batch 1024/4096: extended sizes")
+    return res
+
+
+def bench_decode_configs(ssm, dev, stream, hbm_peak):
+    """Decode steps/s at the long-context configurations' own shapes, batch 1: the Falcon-Mamba-
+    like slice (d_inner 2048, 512 steps after its prefill) and the Zamba-like layer (d_inner 7168,
+    16384 steps), each as one CUDA graph of that many back-to-back steps."""
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_decode_inputs, make_mixer_params, make_states
+    res = {}
+    for name, (D, steps) in {"falcon_mamba7b_like_slice_d2048_512_steps": (2048, 512),
+                             "zamba7b_like_d7168_16384_steps": (7168, 16384)}.items():
+        par = {k: v.to(dev) for k, v in make_mixer_params(D, seed=1).items()}
+        tok = {k: v.to(dev) for k, v in make_decode_inputs(1, D, seed=2).items()}
+        cs, ss = (t.to(dev) for t in make_states(1, D, seed=3))
+        out = torch.empty(1, D, device=dev)
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(stream)
+
+        def one():
+            ssm.decode_step(tok["x"], tok["z"], tok["dt"], tok["B"], tok["C"], par["A"], par["D"], par["dt_bias"],
+                            par["conv_w"], par["conv_b"], cs, ss, out=out, stream=s)
+
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                one()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(steps):
+                one()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        res[name] = {"steps_per_s": 1.0 / t, "us_per_step": 1e6 * t, "GB_s": decode_bytes(1, D) / t / 1e9}
+        del g
+    res["note"] = "batch 1, bf16 tokens, fp32 states in place; launch-bound (one 1 x d_inner step per kernel)"
     return res
 
 
