@@ -170,3 +170,18 @@ def test_decode_tokens_slots_and_prefill_continuation():
     assert_rms_close(out, ref["out"][:, L1:], 2e-3, "block after prefill")
     assert_rms_close(ssm_s[slots.long()], ref["ssm_state"], 2e-3, "slot states")
     assert torch.equal(conv[0], torch.zeros(3, D, device=DEV)) and torch.equal(ssm_s[2], torch.zeros(D, 16, device=DEV))
+
+
+def test_decode_tokens_longest_block():
+    """The largest block the ABI accepts, 4096 tokens per request, against the oracle."""
+    batch, T, D = 2, 4096, 32
+    inp = make_mixer_inputs(batch, T, D, dtype=torch.bfloat16, seed=41)
+    cs, ss = make_states(batch, D, seed=42)
+    ref = oracle_prefill(inp, cs, ss)
+    g = inp.to(DEV)
+    gcs, gss = cs.to(DEV), ss.to(DEV)
+    out = ssm.decode_tokens(g.x, g.z, g.dt, g.B, g.C, g.A, g.D, g.dt_bias, g.conv_w, g.conv_b, gcs, gss)
+    torch.cuda.synchronize()
+    assert_parity(out, ref["out"], torch.bfloat16, "4096-token block out")
+    assert_parity(gss, ref["ssm_state"], torch.bfloat16, "4096-token block state")
+    assert np.array_equal(gcs.cpu().double().numpy(), ref["conv_state"])

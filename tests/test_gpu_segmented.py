@@ -124,3 +124,17 @@ def test_batch1_layers_sampled(L, D):
     assert_rms_close(ss.index_select(1, ix), ref["ssm_state"], 2e-3, "ssm_state")
     assert np.array_equal(cs.index_select(2, ix).cpu().double().numpy(), ref["conv_state"])
     assert torch.isfinite(out).all() and ssm.device_status() == 0
+
+
+def test_segmented_bf16_output():
+    """Segments with a bf16 output: the bf16-out bar (2e-3 RMS plus half a bf16 ulp)."""
+    from _gpu import half_ulp_bf16
+    inp = make_mixer_inputs(2, 777, 64, dtype=torch.bfloat16, seed=31)
+    g = inp.to(DEV)
+    out, _, sso = ssm.prefill(g.x, g.z, g.dt, g.B, g.C, g.A, g.D, g.dt_bias, g.conv_w, g.conv_b,
+                              out_dtype=torch.bfloat16, seg_len=192)
+    torch.cuda.synchronize()
+    ref = oracle_prefill(inp)
+    assert out.dtype == torch.bfloat16
+    assert_rms_close(out.float(), ref["out"], 2e-3, "bf16 out", extra=half_ulp_bf16(ref["out"]))
+    assert_rms_close(sso, ref["ssm_state"], 2e-3, "ssm_state")
