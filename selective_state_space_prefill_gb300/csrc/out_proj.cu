@@ -378,12 +378,17 @@ int launch_bn(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, i
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        // as many clusters as can be resident at once (a cluster's two CTAs share a GPC)
-        cfg.gridDim = dim3((unsigned)(2 * (pairs < n_sm / 2 ? pairs : n_sm / 2)));
-        int resident = 0;
-        if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
-            *why = "cudaOccupancyMaxActiveClusters failed";
-            return -1;
+        // as many clusters as can be resident at once (a cluster's two CTAs share a GPC),
+        // asked of the runtime once per device and kept
+        static int resident_by_dev[64] = {0};
+        int resident = __atomic_load_n(&resident_by_dev[dev & 63], __ATOMIC_ACQUIRE);
+        if (resident < 1) {
+            cfg.gridDim = dim3((unsigned)(2 * (pairs < n_sm / 2 ? pairs : n_sm / 2)));
+            if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
+                *why = "cudaOccupancyMaxActiveClusters failed";
+                return -1;
+            }
+            __atomic_store_n(&resident_by_dev[dev & 63], resident, __ATOMIC_RELEASE);
         }
         const int64_t clusters = pairs < resident ? pairs : resident;
         cfg.gridDim = dim3((unsigned)(2 * clusters));
