@@ -273,7 +273,8 @@ int ssm_decode_tokens(int batch, int n_tokens, int d_inner, int d_state, int d_c
  * shared scale is the maximum of the ranks' block_amax.
  *
  *   M, N, K                  rows (batch x tokens), model width, channels of the slice;
- *                            N % 128 == 0, K % 8 == 0, M <= 65535 * 128
+ *                            N % 128 == 0, K % 8 == 0, M <= 65535 * 128, and
+ *                            ceil(M/128) * ceil(N/128) * ceil(K/64) < 2^31
  *   y, ldy                   [M][K] bf16, row stride ldy >= K (a multiple of 8), 16-byte aligned
  *   W, ldw                   [N][K] bf16: the weight's columns for the slice, K contiguous
  *   out_dtype, out, ldo      [M][N] SSM_BF16 (round to nearest even) or SSM_F32, row

@@ -267,6 +267,11 @@ int ssm_out_proj_partial(int64_t M, int64_t N, int64_t K, const void* y, int64_t
         return fail(SSM_ERR_MISALIGNED, "%s: row strides must be multiples of 8 elements", fn);
     if (!aligned(y, 16) || !aligned(W, 16) || !aligned(out, 16) || (block_amax && !aligned(block_amax, 4)))
         return fail(SSM_ERR_MISALIGNED, "%s: y, W and out must be 16-byte aligned", fn);
+    // the kernel counts 128-row tiles and 64-wide K steps in 32 bits
+    const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    if (tiles * ((K + 63) / 64) >= (1LL << 31))
+        return fail(SSM_ERR_UNSUPPORTED, "%s: %lld tiles x %lld K steps exceed 2^31", fn, (long long)tiles,
+                    (long long)((K + 63) / 64));
 
     int serr = 0;
     unsigned int* status = status_ptr(&serr);

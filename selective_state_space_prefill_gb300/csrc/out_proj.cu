@@ -153,23 +153,22 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
     __shared__ int s_err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // tile counts and indices in 64 bits: up to 65535 x 65535 tiles are accepted
-    const int64_t n_tiles = (p.N + kBN - 1) / kBN;
-    const int64_t m_tiles = (p.M + kBM - 1) / kBM;
+    const int n_tiles = (int)((p.N + kBN - 1) / kBN);
+    const int m_tiles = (int)((p.M + kBM - 1) / kBM);
     const int nk = (int)((p.K + kBK - 1) / kBK);
     const int rank = kPair ? (int)(blockIdx.x & 1) : 0;
     // this CTA's i-th tile: false when there is none; *m0, *n0 its origin
-    auto tile = [&](int64_t i, int* m0, int* n0) -> bool {
+    auto tile = [&](int i, int* m0, int* n0) -> bool {
         if (kPair) {
-            const int64_t pt = (int64_t)(blockIdx.x >> 1) + i * (int64_t)(gridDim.x >> 1);
+            const int pt = (int)(blockIdx.x >> 1) + i * (int)(gridDim.x >> 1);
             if (pt >= n_tiles * ((m_tiles + 1) / 2)) return false;
-            *m0 = (int)((2 * (pt / n_tiles) + rank) * kBM);
-            *n0 = (int)((pt % n_tiles) * kBN);
+            *m0 = (2 * (pt / n_tiles) + rank) * kBM;
+            *n0 = (pt % n_tiles) * kBN;
         } else {
-            const int64_t t = (int64_t)blockIdx.x + i * (int64_t)gridDim.x;
+            const int t = (int)blockIdx.x + i * (int)gridDim.x;
             if (t >= n_tiles * m_tiles) return false;
-            *m0 = (int)((t / n_tiles) * kBM);
-            *n0 = (int)((t % n_tiles) * kBN);
+            *m0 = (t / n_tiles) * kBM;
+            *n0 = (t % n_tiles) * kBN;
         }
         return true;
     };
@@ -201,11 +200,10 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer, running ahead across tile boundaries
-        int64_t it = 0;
-        int m0, n0;
-        for (int64_t i = 0; !s_err && tile(i, &m0, &n0); ++i) {
+        int it = 0, m0, n0;
+        for (int i = 0; !s_err && tile(i, &m0, &n0); ++i) {
             for (int kb = 0; kb < nk; ++kb, ++it) {
-                const int s = (int)(it % kStages);
+                const int s = it % kStages;
                 if (it >= kStages && !mbar_wait_bounded(&empty[s], (uint32_t)(((it / kStages) + 1) & 1))) {
                     s_err = 1;
                     atomicOr(p.status, 1u);
@@ -223,14 +221,13 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
         }
         // tail: every stage's last use has been released by both CTAs' MMAs, so no arrival is
         // still on its way to this CTA's barriers when it exits
-        for (int64_t u = it - 1; u >= 0 && u >= it - kStages && !s_err; --u)
+        for (int u = it - 1; u >= 0 && u >= it - kStages && !s_err; --u)
             if (!mbar_wait_bounded(&empty[u % kStages], (uint32_t)((u / kStages) & 1))) atomicOr(p.status, 1u);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer: tile i accumulates into TMEM buffer i % 2
-        int64_t it = 0;
-        int m0, n0;
-        for (int64_t tl = 0; !s_err && tile(tl, &m0, &n0); ++tl) {
-            const int buf = (int)(tl & 1);
+        int it = 0, m0, n0;
+        for (int tl = 0; !s_err && tile(tl, &m0, &n0); ++tl) {
+            const int buf = tl & 1;
             if (tl >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((tl / 2) + 1) & 1))) {
                 s_err = 1;
                 atomicOr(p.status, 1u);
@@ -239,7 +236,7 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
             tc_fence_after();
             const uint32_t dt = tmem + (uint32_t)(buf * kBN);
             for (int kb = 0; kb < nk; ++kb, ++it) {
-                const int s = (int)(it % kStages);
+                const int s = it % kStages;
                 if (!mbar_wait_bounded(&full[s], (uint32_t)((it / kStages) & 1))) {
                     s_err = 1;
                     atomicOr(p.status, 1u);
@@ -261,8 +258,8 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
         // ---- epilogue: rows m0 + 32 q + lane of each tile, q = warp % 4
         const int q = warp & 3;
         int m0, n0;
-        for (int64_t tl = 0; tile(tl, &m0, &n0); ++tl) {
-            const int buf = (int)(tl & 1);
+        for (int tl = 0; tile(tl, &m0, &n0); ++tl) {
+            const int buf = tl & 1;
             if (!mbar_wait_bounded(&acc_full[buf], (uint32_t)((tl / 2) & 1))) {
                 atomicOr(p.status, 1u);
                 break;

@@ -187,6 +187,7 @@ def _out_proj(lib, **kw):
     (dict(y=None), INVALID), (dict(N=700, ldo=704), UNSUPPORTED), (dict(K=1540, ldy=1544, ldw=1544), UNSUPPORTED),
     (dict(ldy=1024), INVALID), (dict(ldo=700), INVALID), (dict(ldw=1540), MISALIGNED),
     (dict(y=FAKE + 8), MISALIGNED), (dict(out=FAKE + 4), MISALIGNED), (dict(M=65535 * 128 + 1), INVALID),
+    (dict(M=65535 * 128, N=65536 * 128, ldo=65536 * 128, K=1 << 20, ldy=1 << 20, ldw=1 << 20), UNSUPPORTED),
 ])
 def test_out_proj_rejects_bad_arguments(lib, kw, code):
     assert _out_proj(lib, **kw) == code
