@@ -203,6 +203,25 @@ def pin_softplus_ln2(lib, L=8, Dn=3):
     _close(got["ssm_state"][0], np.repeat((np.log(2.0) * u.sum(0))[:, None], 16, 1), 1e-13, "ln2")
 
 
+def pin_dt_bias_is_softplus_inverse(lib, Dn=16):
+    """dt = 0 with dt_bias = log(expm1(u)): delta = softplus(dt_bias) = u, up to the fp32 rounding of
+    dt_bias (times the slope sigmoid(dt_bias) ~ u).  A = 0, B = 1, x = 1 and the current-token tap only
+    leave h = delta * SiLU(1) after one token."""
+    u = torch.exp(torch.linspace(np.log(1e-3), np.log(1e-1), Dn, dtype=torch.float64))
+    inp = make_mixer_inputs(1, 1, Dn, dtype=torch.float32, seed=43)
+    inp.x = torch.ones_like(inp.x)
+    inp.dt = torch.zeros_like(inp.dt)
+    inp.dt_bias = log_expm1(u).float()
+    inp.A = torch.zeros(Dn, 16)
+    inp.B = torch.ones_like(inp.B)
+    inp.conv_w = torch.tensor([[0.0, 0.0, 0.0, 1.0]]).repeat(Dn, 1)
+    inp.conv_b = torch.zeros(Dn)
+    got = _run_prefill(lib, inp)
+    delta = got["ssm_state"][0][:, 0] / expit(1.0)
+    b64 = log_expm1(u).numpy()
+    slack = np.abs(inp.dt_bias.double().numpy() - b64) * expit(b64) * 1.01 + 1e-15
+    assert np.all(np.abs(delta - u.numpy()) <= slack + 1e-13 * u.numpy()), (delta, u)
+
 def pin_state_caching(lib, L1=21, L2=11, Dn=6, dtype=torch.float32):
     """Methodology 3: prefill(L1) then L2 decode steps equals prefill(L1 + L2)."""
     inp = make_mixer_inputs(2, L1 + L2, Dn, dtype=dtype, seed=51)
@@ -361,7 +380,8 @@ def pin_out_proj_identity_and_rank_one(lib):
     assert np.array_equal(r["out"], np.outer(u, pn) * float(v @ q)), "rank one"
 
 MIXER_PINS = [pin_brute_force, pin_brute_force_bf16, pin_short_sequence, pin_prefix_sum_A_zero,
-              pin_geometric_series, pin_C_zero_skip_gate, pin_softplus_ln2, pin_state_caching,
+              pin_geometric_series, pin_C_zero_skip_gate, pin_softplus_ln2, pin_dt_bias_is_softplus_inverse,
+              pin_state_caching,
               pin_decode_matches_brute, pin_split_invariance]
 SCAN_PINS = [pin_scan_sequential, pin_scan_chunked]
 Q8_PINS = [pin_q8_hand_cases, pin_q8_bounds]
