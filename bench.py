@@ -338,6 +338,28 @@ def run_ours(args):
         t1 = time.perf_counter() - t1
         cpu["one_thread_value"] = B * L * n1 / D / t1
         cpu["one_thread_sample"] = f"{n1} of {D} channels x {B} x {L} tokens on 1 thread in {t1:.2f} s"
+        # the other configurations on the same cores, on channel samples (channels are independent,
+        # so a layer's rate is the sample's rate scaled by the channel ratio)
+        from selective_state_space_prefill_gb300.inputs import make_decode_inputs, make_mixer_params, make_states
+        other = {}
+        for name, (Lo, Do, ds) in {"falcon_mamba7b_like_slice_L16384_d2048": (16384, 2048, 128),
+                                   "zamba7b_like_L65536_d7168": (65536, 7168, 64)}.items():
+            smp = make_mixer_inputs(1, Lo, ds, dtype=torch.bfloat16, seed=0)
+            t2 = time.perf_counter()
+            _orc.prefill(smp.x, smp.z, smp.dt, smp.B, smp.C, smp.A, smp.D, smp.dt_bias, smp.conv_w, smp.conv_b,
+                         n_threads=threads)
+            t2 = time.perf_counter() - t2
+            other[name] = {"tokens_per_s": Lo * ds / Do / t2, "sample": f"{ds} of {Do} channels, {t2:.2f} s"}
+        Bd, Dd = 256, 8192
+        tok = make_decode_inputs(Bd, Dd, seed=Bd)
+        par = make_mixer_params(Dd, seed=1)
+        cs0, ss0 = make_states(Bd, Dd, seed=Bd)
+        t3 = time.perf_counter()
+        _orc.decode_step(tok["x"], tok["z"], tok["dt"], tok["B"], tok["C"], par["A"], par["D"], par["dt_bias"],
+                         par["conv_w"], par["conv_b"], cs0, ss0)
+        t3 = time.perf_counter() - t3
+        other["decode_batch256_d8192"] = {"steps_per_s": 1.0 / t3, "sample": f"one whole step, {t3:.3f} s"}
+        cpu["other_workloads"] = other
 
     if rank == 0:
         line = {
