@@ -342,8 +342,8 @@ def run_ours(args):
         # so a layer's rate is the sample's rate scaled by the channel ratio)
         from selective_state_space_prefill_gb300.inputs import make_decode_inputs, make_mixer_params, make_states
         other = {}
-        for name, (Lo, Do, ds) in {"falcon_mamba7b_like_slice_L16384_d2048": (16384, 2048, 128),
-                                   "zamba7b_like_L65536_d7168": (65536, 7168, 64)}.items():
+        for name, (Lo, Do, ds) in {"falcon_mamba7b_like_slice_L16384_d2048": (16384, 2048, 512),
+                                   "zamba7b_like_L65536_d7168": (65536, 7168, 256)}.items():
             smp = make_mixer_inputs(1, Lo, ds, dtype=torch.bfloat16, seed=0)
             t2 = time.perf_counter()
             _orc.prefill(smp.x, smp.z, smp.dt, smp.B, smp.C, smp.A, smp.D, smp.dt_bias, smp.conv_w, smp.conv_b,
