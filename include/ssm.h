@@ -317,6 +317,16 @@ int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype,
                        float* scales_out, void* cuda_stream);
 
 /*
+ * ssm_selftest_expire_wait -- a diagnostic with no counterpart in the pages: launches one
+ * kernel that waits, through the library's bounded mbarrier wait, for a phase that nothing
+ * completes.  After limit_us microseconds (1 .. 2e6) the wait gives up, the kernel sets
+ * SSM_DEV_WAIT_TIMEOUT in the device status word and returns normally.  It shows on a given
+ * GPU that an expired in-kernel wait is reported through ssm_device_status and that the
+ * context stays usable, without faulting or hanging the GPU.
+ */
+int ssm_selftest_expire_wait(int limit_us, void* cuda_stream);
+
+/*
  * ssm_device_status -- read (and if `clear` is nonzero, reset) the device status
  * word of the current device: an OR of SSM_DEV_* bits set by kernels that hit a
  * bounded-wait timeout or a bad state slot since the last clear.  Synchronises

@@ -22,7 +22,7 @@ DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
 
 EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_segmented",
            "ssm_prefill_segmented_noalloc", "ssm_decode_step", "ssm_decode_tokens", "ssm_out_proj_partial",
-           "q8_reduce_partials", "ssm_device_status", "ssm_last_error")
+           "q8_reduce_partials", "ssm_selftest_expire_wait", "ssm_device_status", "ssm_last_error")
 NOALLOC_SCRATCH_BYTES = 4 << 20     # SSM_NOALLOC_SCRATCH_BYTES
 
 
@@ -69,6 +69,8 @@ def load(path: Path | str | None = None):
     lib.ssm_out_proj_partial.restype = I
     lib.q8_reduce_partials.argtypes = [I, P, I, L, I, P, I, P, P, P]
     lib.q8_reduce_partials.restype = I
+    lib.ssm_selftest_expire_wait.argtypes = [I, P]
+    lib.ssm_selftest_expire_wait.restype = I
     lib.ssm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
     lib.ssm_device_status.restype = I
     if path is None:
@@ -357,3 +359,9 @@ def out_proj_partial(y, W, out=None, out_dtype=torch.bfloat16, block_amax=True, 
                                   _ptr(out), out.stride(0), _ptr(amax), _stream(stream))
     _check(lib, "ssm_out_proj_partial", rc)
     return out, amax
+
+
+def selftest_expire_wait(limit_us: int = 50000, stream=None) -> None:
+    """ssm_selftest_expire_wait: one kernel whose bounded wait expires after limit_us."""
+    lib = load()
+    _check(lib, "ssm_selftest_expire_wait", lib.ssm_selftest_expire_wait(int(limit_us), _stream(stream)))

@@ -191,7 +191,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
 
 extern "C" {
 
-int ssm_abi_version(void) { return 103; }
+int ssm_abi_version(void) { return 104; }
 
 const char* ssm_last_error(void) { return g_err; }
 
@@ -286,6 +286,19 @@ int ssm_out_proj_partial(int64_t M, int64_t N, int64_t K, const void* y, int64_t
     a.status = status;
     const char* why = "";
     if (ssm::launch_out_proj(a, y, W, ldy, ldw, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
+    return SSM_OK;
+}
+
+int ssm_selftest_expire_wait(int limit_us, void* cuda_stream) {
+    static const char* fn = "ssm_selftest_expire_wait";
+    g_err[0] = 0;
+    if (limit_us < 1 || limit_us > 2000000) return fail(SSM_ERR_INVALID_ARG, "%s: limit_us %d not in [1, 2e6]", fn, limit_us);
+    int serr = 0;
+    unsigned int* status = status_ptr(&serr);
+    if (serr) return fail(SSM_ERR_CUDA, "%s: no usable CUDA device", fn);
+    const char* why = "";
+    if (ssm::launch_expire_wait(status, (uint64_t)limit_us * 1000u, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
         return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
     return SSM_OK;
 }

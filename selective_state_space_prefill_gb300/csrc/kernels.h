@@ -76,6 +76,7 @@ struct OutProjArgs {
 int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why);
 int launch_decode(const DecodeArgs& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
 int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
+int launch_expire_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream, const char** why);
 int launch_out_proj(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, int64_t ldw, bool out_bf16,
                     cudaStream_t stream, const char** why);
 

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding.EXPORTS)
     for fn in names:
         assert hasattr(lib, fn), fn
-    assert lib.ssm_abi_version() == 103
+    assert lib.ssm_abi_version() == 104
 
 
 FAKE = 0x10000  # 64 KiB-aligned fake device address, never dereferenced
@@ -192,3 +192,8 @@ def _out_proj(lib, **kw):
 def test_out_proj_rejects_bad_arguments(lib, kw, code):
     assert _out_proj(lib, **kw) == code
     assert lib.ssm_last_error().decode().startswith("ssm_out_proj_partial")
+
+
+@pytest.mark.parametrize("limit", [0, -5, 2000001])
+def test_selftest_rejects_bad_limits(lib, limit):
+    assert lib.ssm_selftest_expire_wait(limit, None) == INVALID
