@@ -29,7 +29,25 @@ from pathlib import Path
 ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
-WORKLOAD = dict(name="mamba130m_like_prefill", batch=4, seqlen=2048, d_inner=1536, d_state=16, d_conv=4)
+# The timed step's workload (--workload); the default is the Mamba-130M-like layer.
+WORKLOADS = {
+    "mamba130m_like_prefill": dict(batch=4, seqlen=2048, d_inner=1536, dtype="bf16"),
+    "tiny_mixer_fp32": dict(batch=1, seqlen=256, d_inner=64, dtype="fp32"),
+    "falcon_mamba7b_like_slice_prefill": dict(batch=1, seqlen=16384, d_inner=2048, dtype="bf16"),
+    "zamba7b_like_long_context_prefill": dict(batch=1, seqlen=65536, d_inner=7168, dtype="bf16"),
+}
+DEFAULT_WORKLOAD = "mamba130m_like_prefill"
+WORKLOAD = dict(name=DEFAULT_WORKLOAD, d_state=16, d_conv=4, **WORKLOADS[DEFAULT_WORKLOAD])
+
+
+def _set_workload(name):
+    global WORKLOAD
+    WORKLOAD = dict(name=name, d_state=16, d_conv=4, **WORKLOADS[name])
+
+
+def _wdtype(w):
+    import torch
+    return torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
 METRIC = "prefill tokens/s and decode steps/s per layer; achieved HBM GB/s vs 8 TB/s"
 UNIT = "tokens/s"
 
@@ -197,7 +215,7 @@ def run_reference(args):
     from selective_state_space_prefill_gb300.inputs import make_mixer_inputs
     import oracle
     w = WORKLOAD
-    inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=torch.bfloat16, seed=0)
+    inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=_wdtype(w), seed=0)
     threads = _host_cores()
     oracle.build()
     for _ in range(args.warmup):
@@ -216,7 +234,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) tokens, Mamba-style parameters)",
         "config": {"workload": w["name"], "batch": w["batch"], "seq_len": w["seqlen"], "d_inner": w["d_inner"],
-                   "d_state": 16, "d_conv": 4, "inputs": "bf16"},
+                   "d_state": 16, "d_conv": 4, "inputs": w["dtype"]},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": "the whole workload (all 1536 channels x 4 x 2048 tokens) per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -248,7 +266,8 @@ def run_ours(args):
 
     w = WORKLOAD
     B, L, D = w["batch"], w["seqlen"], w["d_inner"]
-    inp = make_mixer_inputs(B, L, D, dtype=torch.bfloat16, seed=0, device=dev)
+    in_es = 2 if w["dtype"] == "bf16" else 4
+    inp = make_mixer_inputs(B, L, D, dtype=_wdtype(w), seed=0, device=dev)
     out = torch.empty(B, L, D, device=dev, dtype=torch.float32)
     cso = torch.empty(B, 3, D, device=dev)
     sso = torch.empty(B, D, 16, device=dev)
@@ -289,7 +308,7 @@ def run_ours(args):
 
     # ---- roofline of the prefill kernel (the only kernel of the step)
     hbm_peak, peak_kind = _peaks()
-    abytes = prefill_bytes(B, L, D)
+    abytes = prefill_bytes(B, L, D, in_es=in_es)
     avg_s = statistics.mean(step_ms) / 1e3
     achieved_gbs = abytes / avg_s / 1e9
     props = torch.cuda.get_device_properties(dev)
@@ -299,7 +318,8 @@ def run_ours(args):
     fp32_peak = n_sm * 128 * sm_max * 1e6 / 1e12           # TFLOP/s-equivalent: FP32-pipe lane-ops/s
     fp32_ach = prefill_fp32_ops(B, L, D) / avg_s / 1e12
     roofline = {"bound": "alu", "achieved": fp32_ach, "peak": fp32_peak, "unit": "T fp32-ops/s",
-                "frac": fp32_ach / fp32_peak, "traffic": _prefill_traffic(), "traffic_unit": "DRAM bytes per launch (ncu)",
+                "frac": fp32_ach / fp32_peak, "traffic": _prefill_traffic() if w["name"] == DEFAULT_WORKLOAD else None,
+                "traffic_unit": "DRAM bytes per launch (ncu)",
                 "kernel": "k_prefill", "peak_source": f"{n_sm} SMs x 128 FP32 lanes x {sm_max:.0f} MHz",
                 "hbm": {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                         "frac": achieved_gbs / hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
@@ -331,7 +351,7 @@ def run_ours(args):
                "sample": f"the whole workload (all {D} channels x {B} x {L} tokens), {reps} run(s) in {el:.1f} s"}
         # one host thread on a channel sample (channels are independent, so the rate scales)
         import oracle as _orc
-        n1 = 96
+        n1 = min(96, D)
         t1 = time.perf_counter()
         _orc.prefill(cpu_inp.x, cpu_inp.z, cpu_inp.dt, cpu_inp.B, cpu_inp.C, cpu_inp.A, cpu_inp.D, cpu_inp.dt_bias,
                      cpu_inp.conv_w, cpu_inp.conv_b, channels=list(range(n1)), n_threads=1)
@@ -368,7 +388,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded N(0,1) tokens; A=-(n+1), D=1, log-uniform dt_bias, U(-.5,.5) conv)",
             "config": {"workload": w["name"], "batch": B, "seq_len": L, "d_inner": D, "d_state": 16, "d_conv": 4,
-                       "inputs": "bf16 x/z/dt/B/C, fp32 params and states", "out": "fp32",
+                       "inputs": f"{w['dtype']} x/z/dt/B/C, fp32 params and states", "out": "fp32",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "flushed before every timed step (write of a 2x-L2 buffer)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -738,7 +758,7 @@ def run_profile_target(which: str):
     dev = torch.device("cuda", 0)
     if which == "prefill":
         w = WORKLOAD
-        inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=torch.bfloat16, seed=0, device=dev)
+        inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=_wdtype(w), seed=0, device=dev)
         for _ in range(4):
             ssm.prefill(inp.x, inp.z, inp.dt, inp.B, inp.C, inp.A, inp.D, inp.dt_bias, inp.conv_w, inp.conv_b)
     elif which == "prefill_seg":
@@ -778,12 +798,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD,
+                    help="the prefill workload of the timed step (default: the Mamba-130M-like layer)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8", "out_proj"], default=None,
                     help="only launch one kernel 4 times (for an ncu capture) and exit")
     args = ap.parse_args()
+    _set_workload(args.workload)
     if args.profile:
         run_profile_target(args.profile)
     elif args.impl == "reference":
