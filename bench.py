@@ -236,7 +236,8 @@ def run_reference(args):
         "config": {"workload": w["name"], "batch": w["batch"], "seq_len": w["seqlen"], "d_inner": w["d_inner"],
                    "d_state": 16, "d_conv": 4, "inputs": w["dtype"]},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "the whole workload (all 1536 channels x 4 x 2048 tokens) per step"},
+                         "sample": f"the whole workload (all {w['d_inner']} channels x {w['batch']} x "
+                                   f"{w['seqlen']} tokens) per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
