@@ -66,11 +66,19 @@ k_decode(const DecodeArgs p) {
     const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)d * 4);
     const float cb = p.conv_b[d], Dd = p.Dskip[d], bias = p.dt_bias[d];
 
+    // the next token's x, z, dt are loaded while the current one is computed
+    const Tin* xg = reinterpret_cast<const Tin*>(p.x) + (int64_t)r * p.in_stride_b + d;
+    const Tin* zg = reinterpret_cast<const Tin*>(p.z) + (int64_t)r * p.in_stride_b + d;
+    const Tin* dg = reinterpret_cast<const Tin*>(p.dt) + (int64_t)r * p.in_stride_b + d;
+    Tin xn = xg[0], zn = zg[0], dn = dg[0];
     for (int t = 0; t < p.n_tokens; ++t) {
-        const int64_t ro = (int64_t)r * p.in_stride_b + (int64_t)t * p.in_stride_t + d;
-        const float xt = to_f32(reinterpret_cast<const Tin*>(p.x)[ro]);
-        const float zt = to_f32(reinterpret_cast<const Tin*>(p.z)[ro]);
-        const float dtt = to_f32(reinterpret_cast<const Tin*>(p.dt)[ro]);
+        const float xt = to_f32(xn), zt = to_f32(zn), dtt = to_f32(dn);
+        if (t + 1 < p.n_tokens) {
+            const int64_t o = (int64_t)(t + 1) * p.in_stride_t;
+            xn = xg[o];
+            zn = zg[o];
+            dn = dg[o];
+        }
         const Tin* Bm = reinterpret_cast<const Tin*>(p.Bm) + ((int64_t)r * p.n_tokens + t) * 16;
         const Tin* Cm = reinterpret_cast<const Tin*>(p.Cm) + ((int64_t)r * p.n_tokens + t) * 16;
 
