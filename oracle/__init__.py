@@ -1,5 +1,5 @@
-"""fp64 CPU oracle for the selective-SSM mixer and its output-projection partial
-(test infrastructure only).
+"""fp64 CPU oracle for the selective-SSM mixer, its SSD (Mamba-2-style) variant and the
+output-projection partial (test infrastructure only).
 
 Only the test-suite, the smoke check and the benchmark's CPU-baseline leg may
 import this package.  It shares no code with the CUDA path: the arithmetic
@@ -19,4 +19,5 @@ from .oracle import (  # noqa: F401
     q8_reduce,
     scan_chunked,
     scan_sequential,
+    ssd_prefill,
 )

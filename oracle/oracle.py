@@ -58,6 +58,9 @@ def _bind(lib):
     lib.oracle_q8_reduce.restype = I
     lib.oracle_out_proj.argtypes = [L, L, L, I, P, P, P, P, P, I]
     lib.oracle_out_proj.restype = I
+    lib.oracle_ssd_prefill.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I,
+                                       P, P, P, I]
+    lib.oracle_ssd_prefill.restype = I
     return lib
 
 
@@ -255,3 +258,40 @@ def out_proj(y, W, n_threads=None, lib=None):
     if rc != 0:
         raise ValueError("oracle_out_proj rejected its arguments")
     return dict(out=out, amax=amax, absdot=absdot)
+
+
+def ssd_prefill(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, n_heads, head_dim, n_groups, d_state,
+                conv_state_in=None, ssm_state_in=None, heads=None, n_threads=None, lib=None):
+    """Oracle prefill of the SSD (Mamba-2-style) mixer.
+
+    xBC [batch, L, H*P + 2*G*N] (channels x | B | C), z [batch, L, H*P], dt [batch, L, H];
+    conv_w [Cx, W], conv_b [Cx], A / D / dt_bias [H] (float32); optional float64 states
+    conv_state_in [batch, W-1, Cx] and ssm_state_in [batch, H, P, N].  ``heads`` (optional
+    index list) evaluates only those heads; the other heads' outputs, states and x conv
+    channels are left NaN.
+    Returns dict(out [b, L, H*P], conv_state [b, W-1, Cx], ssm_state [b, H, P, N]) in float64.
+    """
+    lib = lib or load()
+    xr, code = _raw(xBC)
+    zr, code_z = _raw(z)
+    dtr, code_dt = _raw(dt)
+    if len({code, code_z, code_dt}) != 1:
+        raise TypeError("xBC, z, dt must share one dtype")
+    conv_w, conv_b, A, D, dt_bias = map(_f32, (conv_w, conv_b, A, D, dt_bias))
+    csi, ssi = _f64(conv_state_in), _f64(ssm_state_in)
+    H, P, G, N = int(n_heads), int(head_dim), int(n_groups), int(d_state)
+    batch, L, Cx = xr.shape
+    if Cx != H * P + 2 * G * N or zr.shape != (batch, L, H * P) or dtr.shape != (batch, L, H):
+        raise ValueError("inconsistent SSD shapes")
+    W = conv_w.shape[-1]
+    hl = None if heads is None else np.ascontiguousarray(np.asarray(heads, dtype=np.int32))
+    out = np.full((batch, L, H * P), np.nan)
+    cso = np.full((batch, W - 1, Cx), np.nan)
+    sso = np.full((batch, H, P, N), np.nan)
+    rc = lib.oracle_ssd_prefill(batch, L, H, P, G, N, W, code, _p(xr), _p(zr), _p(dtr), _p(conv_w),
+                                _p(conv_b), _p(A), _p(D), _p(dt_bias), _p(csi), _p(ssi), _p(hl),
+                                0 if hl is None else int(hl.size), _p(out), _p(cso), _p(sso),
+                                _threads(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_prefill rejected its arguments (rc={rc})")
+    return dict(out=out, conv_state=cso, ssm_state=sso)

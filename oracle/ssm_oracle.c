@@ -17,6 +17,8 @@
  *     the hidden state and decode continues from it without recomputing tokens.
  *   - Methodology 4 ("quantized All-Reduce"): partial outputs are quantized to
  *     8 bits before they are summed and dequantized afterwards.
+ * The last function, oracle_ssd_prefill, is the Mamba-2-style (SSD) variant of the
+ * same mixer; its own header states its source and readings.
  * The pages do not print the mixer's equations.  This file uses the
  * Mamba-style selective-scan mixer (width-4 causal depthwise conv + SiLU,
  * softplus step, diagonal recurrence, C readout, D skip, SiLU(z) gate), with
@@ -40,6 +42,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -349,4 +352,126 @@ int oracle_out_proj(int64_t M, int64_t N, int64_t K, int in_dtype, const void* y
         }
     }
     return 0;
+}
+
+/*
+ * oracle_ssd_prefill -- the structured-state-space-duality (SSD, Mamba-2-style)
+ * variant of the mixer: the same local recurrence, with the decay a scalar per
+ * head and B, C shared by the heads of a group.  The pages name the model
+ * families this serves (Overview: Mamba, Falcon-Mamba and Zamba) but print no
+ * equations for this form; it follows the published Mamba-2 layer (Dao and Gu,
+ * "Transformers are SSMs", 2024), with these readings:
+ *   - one width-W causal depthwise conv + SiLU runs over the concatenated input
+ *     channels [x | B | C] (Cx = H*P + 2*G*N per token): channel h*P + p is x of
+ *     head h, position p; H*P + g*N + n is B of group g; H*P + G*N + g*N + n is C;
+ *   - head h belongs to group g(h) = h / (H / G) (contiguous blocks of heads);
+ *   - Delta = softplus(dt + dt_bias[h]) per token and head; the decay is
+ *     exp(Delta * A[h]);
+ *   - state S[h][p][n] <- exp(Delta A[h]) S[h][p][n] + Delta x[h][p] B[g(h)][n];
+ *   - y[h][p] = sum_n C[g(h)][n] S[h][p][n] + D[h] x[h][p], out = y * SiLU(z);
+ *   - the gated normalisation that follows in Mamba-2 is a separate layer op and
+ *     is not part of this mixer, like the output projection.
+ * Every step is the definition written out in double precision, token by token.
+ *   xBC [batch][L][Cx], z [batch][L][H*P], dt [batch][L][H]   in_dtype
+ *   conv_w [Cx][W], conv_b [Cx], A [H], Dskip [H], dt_bias [H]  float32
+ *   conv_state_in  [batch][W-1][Cx]  float64 or NULL (zeros), raw inputs, oldest first
+ *   ssm_state_in   [batch][H][P][N]  float64 or NULL (zeros)
+ *   heads          n_run head indices to evaluate, or NULL for all H heads; only their
+ *                  rows of out / ssm_state_out and their x channels of
+ *                  conv_state_out are written (B and C channels always are)
+ * Outputs (float64): out [batch][L][H*P], conv_state_out [batch][W-1][Cx],
+ * ssm_state_out [batch][H][P][N].  Returns 0, or -1 on a bad size.
+ */
+int oracle_ssd_prefill(int batch, int L, int H, int P, int G, int N, int W, int in_dtype,
+                       const void* xBC, const void* z, const void* dt,
+                       const float* conv_w, const float* conv_b,
+                       const float* A, const float* Dskip, const float* dt_bias,
+                       const double* conv_state_in, const double* ssm_state_in,
+                       const int* heads, int n_run,
+                       double* out, double* conv_state_out, double* ssm_state_out, int n_threads)
+{
+    if (batch < 0 || L < 0 || H < 1 || P < 1 || G < 1 || N < 1 || W < 1 || W > 64) return -1;
+    if (H % G != 0) return -1;
+    if (!heads) n_run = H;
+    if (n_threads < 1) n_threads = 1;
+    const int64_t Cx = (int64_t)H * P + 2 * (int64_t)G * N;
+    const int hpg = H / G;
+    const int64_t jobs = (int64_t)batch * n_run;
+    int bad = 0;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+    for (int64_t job = 0; job < jobs; ++job) {
+        const int b = (int)(job / n_run);
+        const int h = heads ? heads[job % n_run] : (int)(job % n_run);
+        if (h < 0 || h >= H) {
+            bad = 1;
+            continue;
+        }
+        const int g = h / hpg;
+        /* the channels this head reads: its P x channels, then its group's N B and N C channels */
+        const int nch = P + 2 * N;
+        int64_t* ch = (int64_t*)malloc(sizeof(int64_t) * nch);
+        double* hist = (double*)malloc(sizeof(double) * nch * (W > 1 ? W - 1 : 1));
+        double* u = (double*)malloc(sizeof(double) * nch);
+        double* S = (double*)malloc(sizeof(double) * (size_t)P * N);
+        if (!ch || !hist || !u || !S) {
+            free(ch); free(hist); free(u); free(S);
+            bad = 1;
+            continue;
+        }
+        for (int p = 0; p < P; ++p) ch[p] = (int64_t)h * P + p;
+        for (int n = 0; n < N; ++n) {
+            ch[P + n] = (int64_t)H * P + (int64_t)g * N + n;
+            ch[P + N + n] = (int64_t)H * P + (int64_t)G * N + (int64_t)g * N + n;
+        }
+        for (int c = 0; c < nch; ++c)
+            for (int k = 0; k < W - 1; ++k)
+                hist[c * (W - 1) + k] = conv_state_in ? conv_state_in[((int64_t)b * (W - 1) + k) * Cx + ch[c]] : 0.0;
+        for (int64_t e = 0; e < (int64_t)P * N; ++e)
+            S[e] = ssm_state_in ? ssm_state_in[((int64_t)b * H + h) * P * N + e] : 0.0;
+
+        for (int t = 0; t < L; ++t) {
+            const int64_t row = (int64_t)b * L + t;
+            /* causal depthwise conv over [hist..., xBC_t] and SiLU, channel by channel */
+            for (int c = 0; c < nch; ++c) {
+                const double xt = widen(xBC, in_dtype, row * Cx + ch[c]);
+                double xc = (double)conv_b[ch[c]];
+                for (int k = 0; k < W - 1; ++k) xc += (double)conv_w[ch[c] * W + k] * hist[c * (W - 1) + k];
+                xc += (double)conv_w[ch[c] * W + W - 1] * xt;
+                u[c] = silu(xc);
+                for (int k = 0; k + 1 < W - 1; ++k) hist[c * (W - 1) + k] = hist[c * (W - 1) + k + 1];
+                if (W > 1) hist[c * (W - 1) + W - 2] = xt;
+            }
+            const double* xh = u;          /* x[h][0..P-1] */
+            const double* Bg = u + P;      /* B[g][0..N-1] */
+            const double* Cg = u + P + N;  /* C[g][0..N-1] */
+            const double delta = softplus(widen(dt, in_dtype, row * H + h) + (double)dt_bias[h]);
+            const double a = exp(delta * (double)A[h]);
+            for (int p = 0; p < P; ++p) {
+                double y = 0.0;
+                for (int n = 0; n < N; ++n) {
+                    S[(int64_t)p * N + n] = a * S[(int64_t)p * N + n] + delta * xh[p] * Bg[n];
+                    y += Cg[n] * S[(int64_t)p * N + n];
+                }
+                y += (double)Dskip[h] * xh[p];
+                const double zt = widen(z, in_dtype, row * H * P + (int64_t)h * P + p);
+                out[row * H * P + (int64_t)h * P + p] = y * silu(zt);
+            }
+        }
+        /* x channels belong to this head; B and C channels are written by the first evaluated
+         * head of the group (every head of a group computes the same B and C history) */
+        int first_of_group = heads ? 1 : (h % hpg == 0);
+        if (heads)
+            for (int64_t q = 0; q < job % n_run; ++q)
+                if (heads[q] >= 0 && heads[q] < H && heads[q] / hpg == g) first_of_group = 0;
+        for (int c = 0; c < nch; ++c) {
+            if (c >= P && !first_of_group) continue;
+            for (int k = 0; k < W - 1; ++k)
+                conv_state_out[((int64_t)b * (W - 1) + k) * Cx + ch[c]] = hist[c * (W - 1) + k];
+        }
+        for (int64_t e = 0; e < (int64_t)P * N; ++e)
+            ssm_state_out[((int64_t)b * H + h) * P * N + e] = S[e];
+        free(ch); free(hist); free(u); free(S);
+    }
+    return bad ? -1 : 0;
 }

@@ -33,6 +33,9 @@ __all__ = [
     "make_states",
     "make_partials",
     "log_expm1",
+    "SSDInputs",
+    "make_ssd_inputs",
+    "make_ssd_states",
 ]
 
 
@@ -142,3 +145,85 @@ def make_out_proj_inputs(M: int, K: int, N: int, dtype=torch.bfloat16, seed: int
     y = torch.randn(M, K, generator=g, device=device, dtype=torch.float32).to(dtype)
     W = (torch.randn(N, K, generator=g, device=device, dtype=torch.float32) / K ** 0.5).to(dtype)
     return y, W
+
+
+@dataclass
+class SSDInputs:
+    """Inputs of the SSD (Mamba-2-style) mixer.
+
+    xBC [batch, L, H*P + 2*G*N] holds the pre-conv channels x (head-major), then B and C
+    of each group; z [batch, L, H*P]; dt [batch, L, H]; per-head A, D, dt_bias [H];
+    per-channel conv_w [Cx, d_conv] and conv_b [Cx].
+    """
+
+    xBC: torch.Tensor
+    z: torch.Tensor
+    dt: torch.Tensor
+    A: torch.Tensor
+    D: torch.Tensor
+    dt_bias: torch.Tensor
+    conv_w: torch.Tensor
+    conv_b: torch.Tensor
+    n_heads: int
+    head_dim: int
+    n_groups: int
+    d_state: int
+
+    _TENSORS = ("xBC", "z", "dt", "A", "D", "dt_bias", "conv_w", "conv_b")
+    _TOKENS = ("xBC", "z", "dt")
+
+    def _kw(self):
+        return {k: getattr(self, k) for k in self.__dataclass_fields__}
+
+    def to(self, device) -> "SSDInputs":
+        kw = self._kw()
+        for k in self._TENSORS:
+            kw[k] = kw[k].to(device)
+        return SSDInputs(**kw)
+
+    def token_slice(self, t0: int, t1: int) -> "SSDInputs":
+        kw = self._kw()
+        for k in self._TOKENS:
+            kw[k] = kw[k][:, t0:t1].contiguous()
+        return SSDInputs(**kw)
+
+    @property
+    def channels(self) -> int:
+        return self.n_heads * self.head_dim + 2 * self.n_groups * self.d_state
+
+
+def make_ssd_inputs(batch: int, seqlen: int, n_heads: int, head_dim: int = 64, n_groups: int = 1,
+                    d_state: int = 64, d_conv: int = 4, dtype: torch.dtype = torch.bfloat16,
+                    seed: int = 0, device="cpu") -> SSDInputs:
+    """Seeded SSD inputs: xBC, z, dt ~ N(0, 1); dt_bias = log(expm1(u_h)) with u_h ~
+    LogUniform[1e-3, 1e-1] per head; A[h] = -U[1, 16] (the usual Mamba-2 initialisation of
+    A = -exp(A_log)); D = 1; conv_w ~ U(-0.5, 0.5); conv_b = 0."""
+    g = _gen(seed + 49979687, device)
+    HP = n_heads * head_dim
+    Cx = HP + 2 * n_groups * d_state
+
+    def normal(*shape):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dtype)
+
+    xBC = normal(batch, seqlen, Cx)
+    z = normal(batch, seqlen, HP)
+    dt = normal(batch, seqlen, n_heads)
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    u = torch.exp(torch.rand(n_heads, generator=g, device=device, dtype=torch.float64) * (hi - lo) + lo)
+    dt_bias = log_expm1(u).float()
+    A = -(1.0 + 15.0 * torch.rand(n_heads, generator=g, device=device, dtype=torch.float32))
+    conv_w = (torch.rand(Cx, d_conv, generator=g, device=device) - 0.5).float().contiguous()
+    return SSDInputs(xBC=xBC, z=z, dt=dt, A=A.contiguous(),
+                     D=torch.ones(n_heads, device=device, dtype=torch.float32), dt_bias=dt_bias,
+                     conv_w=conv_w, conv_b=torch.zeros(Cx, device=device, dtype=torch.float32),
+                     n_heads=n_heads, head_dim=head_dim, n_groups=n_groups, d_state=d_state)
+
+
+def make_ssd_states(batch: int, n_heads: int, head_dim: int, d_state: int, channels: int,
+                    d_conv: int = 4, seed: int = 0, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+    """Cached fp32 SSD states ~ N(0, 1): conv_state [batch, d_conv-1, channels] and
+    ssm_state [batch, n_heads, head_dim, d_state]."""
+    g = _gen(seed + 67867967, device)
+    conv_state = torch.randn(batch, d_conv - 1, channels, generator=g, device=device, dtype=torch.float32)
+    ssm_state = torch.randn(batch, n_heads, head_dim, d_state, generator=g, device=device, dtype=torch.float32)
+    return conv_state, ssm_state

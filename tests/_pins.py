@@ -26,7 +26,8 @@ import torch
 from scipy.special import expit
 
 import oracle.oracle as orc
-from selective_state_space_prefill_gb300.inputs import log_expm1, make_mixer_inputs, make_partials
+from selective_state_space_prefill_gb300.inputs import (log_expm1, make_mixer_inputs, make_partials,
+                                                         make_ssd_inputs)
 
 GOLDEN = Path(__file__).resolve().parent / "golden"
 
@@ -379,6 +380,155 @@ def pin_out_proj_identity_and_rank_one(lib):
     r = orc.out_proj(yy, WW, lib=lib)
     assert np.array_equal(r["out"], np.outer(u, pn) * float(v @ q)), "rank one"
 
+# ----------------------------------------------------------------- SSD (Mamba-2-style) pins
+def _ssd_run(lib, inp, cs=None, ss=None, **kw):
+    return orc.ssd_prefill(inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias,
+                           inp.n_heads, inp.head_dim, inp.n_groups, inp.d_state,
+                           conv_state_in=cs, ssm_state_in=ss, n_threads=2, lib=lib, **kw)
+
+
+def _ssd_conv_silu(inp, cs):
+    """u[b, t, c] = SiLU(conv_b[c] + sum_k conv_w[c, k] xe[b, t + k, c]) over xe = [cs ; xBC]."""
+    x = _np64(inp.xBC)
+    w, cb = _np64(inp.conv_w), _np64(inp.conv_b)
+    batch, L, Cx = x.shape
+    W = w.shape[1]
+    xe = np.concatenate([cs, x], 1)
+    xc = np.broadcast_to(cb, (batch, L, Cx)).copy()
+    for k in range(W):
+        xc += w[:, k][None, None, :] * xe[:, k:k + L, :]
+    return xc * expit(xc), xe
+
+
+def ssd_matrix_form(inp, cs=None, ss=None, chunk=None):
+    """The SSD mixer evaluated through its quadratic ("dual") matrix form, in float64.
+
+    Per batch row and head h (group g = h // (H // G)), with u = SiLU(conv(xBC)):
+      delta_t = logaddexp(0, dt_t + dt_bias_h), s_t = sum_{r <= t} delta_r A_h,
+      M[i, j] = exp(s_i - s_j) (C_i . B_j) for j <= i, else 0,
+      Y = M @ (delta[:, None] x) + exp(s)[:, None] (C @ S0^T) + D_h x,
+      S_L = exp(s_L) S0 + (x * w[:, None])^T B with w_j = exp(s_L - s_j) delta_j,
+      out = Y * z * expit(z).
+    With ``chunk`` the same form is applied chunk by chunk, the state carried between chunks
+    (the chunked algorithm the GPU kernel follows).  Nothing here steps a recurrence token by token.
+    """
+    H, P, G, N = inp.n_heads, inp.head_dim, inp.n_groups, inp.d_state
+    z, dt = _np64(inp.z), _np64(inp.dt)
+    A, D, dtb = _np64(inp.A), _np64(inp.D), _np64(inp.dt_bias)
+    batch, L, Cx = inp.xBC.shape
+    W = inp.conv_w.shape[1]
+    cs = np.zeros((batch, W - 1, Cx)) if cs is None else _np64(cs)
+    ss = np.zeros((batch, H, P, N)) if ss is None else _np64(ss)
+    u, xe = _ssd_conv_silu(inp, cs)
+    out = np.zeros((batch, L, H * P))
+    s_last = np.zeros((batch, H, P, N))
+    Q = L if not chunk else chunk
+    for b in range(batch):
+        for h in range(H):
+            g = h // (H // G)
+            xh = u[b, :, h * P:(h + 1) * P]
+            Bg = u[b, :, H * P + g * N:H * P + (g + 1) * N]
+            Cg = u[b, :, H * P + G * N + g * N:H * P + G * N + (g + 1) * N]
+            delta = np.logaddexp(0.0, dt[b, :, h] + dtb[h])
+            S = ss[b, h].copy()
+            for t0 in range(0, L, max(Q, 1)):
+                t1 = min(L, t0 + Q)
+                dl, xc, Bc, Cc = delta[t0:t1], xh[t0:t1], Bg[t0:t1], Cg[t0:t1]
+                sc = np.cumsum(dl * A[h])
+                diff = sc[:, None] - sc[None, :]
+                M = np.where(np.tril(np.ones((t1 - t0, t1 - t0), bool)), np.exp(np.minimum(diff, 0.0)), 0.0)
+                M = M * (Cc @ Bc.T)
+                Y = M @ (dl[:, None] * xc) + np.exp(sc)[:, None] * (Cc @ S.T) + D[h] * xc
+                out[b, t0:t1, h * P:(h + 1) * P] = Y * z[b, t0:t1, h * P:(h + 1) * P] * expit(
+                    z[b, t0:t1, h * P:(h + 1) * P])
+                w = np.exp(sc[-1] - sc) * dl
+                S = np.exp(sc[-1]) * S + (xc * w[:, None]).T @ Bc
+            s_last[b, h] = S
+    return dict(out=out, conv_state=xe[:, xe.shape[1] - (W - 1):, :], ssm_state=s_last)
+
+
+def _ssd_tiny(seed, dtype=torch.float32, batch=2, L=13, H=4, P=3, G=2, N=5):
+    inp = make_ssd_inputs(batch, L, H, P, G, N, dtype=dtype, seed=seed)
+    g = torch.Generator().manual_seed(seed + 11)
+    inp.conv_b = torch.randn(inp.channels, generator=g) * 0.3
+    inp.D = torch.randn(H, generator=g)
+    cs = torch.randn(batch, 3, inp.channels, generator=g, dtype=torch.float64)
+    ss = torch.randn(batch, H, P, N, generator=g, dtype=torch.float64)
+    return inp, cs, ss
+
+
+def pin_ssd_matrix_form(lib):
+    """Random tiny SSD problems (fp32 and bf16, with input states) against the quadratic form."""
+    for seed, dtype in ((21, torch.float32), (22, torch.bfloat16)):
+        inp, cs, ss = _ssd_tiny(seed, dtype)
+        got = _ssd_run(lib, inp, cs, ss)
+        ref = ssd_matrix_form(inp, cs, ss)
+        for k in ("out", "ssm_state", "conv_state"):
+            _close(got[k], ref[k], 1e-12, f"SSD matrix form {k} ({dtype})")
+
+
+def pin_ssd_chunked_state_passing(lib):
+    """The chunk-by-chunk form with the state carried across chunks equals the oracle for
+    chunk sizes 1, 4, 7 and L (and a ragged last chunk)."""
+    inp, cs, ss = _ssd_tiny(23, batch=1, L=17, H=2, P=4, G=1, N=6)
+    got = _ssd_run(lib, inp, cs, ss)
+    for q in (1, 4, 7, 17):
+        ref = ssd_matrix_form(inp, cs, ss, chunk=q)
+        for k in ("out", "ssm_state"):
+            _close(got[k], ref[k], 1e-12, f"SSD chunk {q} {k}")
+
+
+def pin_ssd_state_caching(lib, L1=11, L2=9):
+    """Prefill of L1 tokens, then of L2 more from the returned states, equals one prefill of L1 + L2."""
+    inp, cs, ss = _ssd_tiny(24, batch=2, L=L1 + L2, H=4, P=3, G=2, N=4)
+    full = _ssd_run(lib, inp, cs, ss)
+    first = _ssd_run(lib, inp.token_slice(0, L1), cs, ss)
+    second = _ssd_run(lib, inp.token_slice(L1, L1 + L2), first["conv_state"], first["ssm_state"])
+    _close(np.concatenate([first["out"], second["out"]], 1), full["out"], 1e-12, "SSD caching out")
+    _close(second["ssm_state"], full["ssm_state"], 1e-12, "SSD caching ssm_state")
+    _close(second["conv_state"], full["conv_state"], 0.0, "SSD caching conv_state")
+
+
+def pin_ssd_reduces_to_mamba1(lib, L=15, H=6, N=5):
+    """With one position per head (P = 1), one group and identity convs on the B and C
+    channels, the SSD mixer is the selective-scan mixer with A[d, n] = A[h] for every n and
+    B, C replaced by SiLU(B), SiLU(C): the two oracles must agree (fp32 rounding of the
+    SiLU'd B and C handed to the selective-scan oracle is the only difference)."""
+    inp = make_ssd_inputs(1, L, H, 1, 1, N, dtype=torch.float32, seed=25)
+    w = inp.conv_w.clone()
+    w[H:] = torch.tensor([0.0, 0.0, 0.0, 1.0])
+    inp.conv_w = w
+    got = _ssd_run(lib, inp)
+    xBC = _np64(inp.xBC)
+    Bs = torch.from_numpy(xBC[..., H:H + N] * expit(xBC[..., H:H + N])).float()
+    Cs = torch.from_numpy(xBC[..., H + N:] * expit(xBC[..., H + N:])).float()
+    m1 = orc.prefill(inp.xBC[..., :H].contiguous(), inp.z, inp.dt, Bs, Cs,
+                     inp.A[:, None].expand(H, N).contiguous(), inp.D, inp.dt_bias,
+                     inp.conv_w[:H].contiguous(), inp.conv_b[:H].contiguous(), n_threads=2)
+    _close(got["out"], m1["out"], 1e-6, "SSD vs selective scan out")
+    _close(got["ssm_state"][..., 0, :], m1["ssm_state"], 1e-6, "SSD vs selective scan state")
+
+
+def pin_ssd_heads_subset(lib):
+    """Evaluating a subset of heads gives exactly those heads of the full run (and NaN elsewhere)."""
+    inp, cs, ss = _ssd_tiny(26, batch=2, L=10, H=6, P=2, G=3, N=3)
+    full = _ssd_run(lib, inp, cs, ss)
+    part = _ssd_run(lib, inp, cs, ss, heads=[4, 1])
+    P = inp.head_dim
+    for h in (1, 4):
+        assert np.array_equal(part["out"][..., h * P:(h + 1) * P], full["out"][..., h * P:(h + 1) * P])
+        assert np.array_equal(part["ssm_state"][:, h], full["ssm_state"][:, h])
+    assert np.isnan(part["out"][..., 0]).all()
+    HP, N, G = inp.n_heads * P, inp.d_state, inp.n_groups
+    for g in (0, 2):                      # the groups of heads 1 and 4 (two heads per group)
+        for base in (HP + g * N, HP + G * N + g * N):
+            assert np.array_equal(part["conv_state"][..., base:base + N], full["conv_state"][..., base:base + N])
+    assert np.isnan(part["conv_state"][..., HP + N:HP + 2 * N]).all()
+
+
+SSD_PINS = [pin_ssd_matrix_form, pin_ssd_chunked_state_passing, pin_ssd_state_caching,
+            pin_ssd_reduces_to_mamba1, pin_ssd_heads_subset]
+
 MIXER_PINS = [pin_brute_force, pin_brute_force_bf16, pin_short_sequence, pin_prefix_sum_A_zero,
               pin_geometric_series, pin_C_zero_skip_gate, pin_softplus_ln2, pin_dt_bias_is_softplus_inverse,
               pin_state_caching,
@@ -386,4 +536,4 @@ MIXER_PINS = [pin_brute_force, pin_brute_force_bf16, pin_short_sequence, pin_pre
 SCAN_PINS = [pin_scan_sequential, pin_scan_chunked]
 Q8_PINS = [pin_q8_hand_cases, pin_q8_bounds]
 OUT_PROJ_PINS = [pin_out_proj_vs_matmul, pin_out_proj_identity_and_rank_one]
-ALL_PINS = MIXER_PINS + SCAN_PINS + Q8_PINS + OUT_PROJ_PINS
+ALL_PINS = MIXER_PINS + SCAN_PINS + Q8_PINS + OUT_PROJ_PINS + SSD_PINS

@@ -50,6 +50,22 @@ MUTATIONS = {
                               "for (int64_t k = 0; k < K - 1; ++k) {\n                const double yv"),
     "out_proj_absdot_signed": ("a += fabs(yv) * fabs(wv);", "a += yv * wv;"),
     "out_proj_amax_signed": ("if (fabs(out[i]) > mx) mx = fabs(out[i]);", "if (out[i] > mx) mx = out[i];"),
+    "ssd_group_interleaved": ("const int g = h / hpg;", "const int g = h % G;"),
+    "ssd_decay_of_group": ("const double a = exp(delta * (double)A[h]);", "const double a = exp(delta * (double)A[g]);"),
+    "ssd_input_drops_delta": ("+ delta * xh[p] * Bg[n];", "+ xh[p] * Bg[n];"),
+    "ssd_readout_uses_B": ("y += Cg[n] * S[(int64_t)p * N + n];", "y += Bg[n] * S[(int64_t)p * N + n];"),
+    "ssd_C_reads_B_channels": ("ch[P + N + n] = (int64_t)H * P + (int64_t)G * N + (int64_t)g * N + n;",
+                               "ch[P + N + n] = (int64_t)H * P + (int64_t)g * N + n;"),
+    "ssd_skip_dropped": ("y += (double)Dskip[h] * xh[p];", "y += 0.0 * xh[p];"),
+    "ssd_dt_of_head_zero": ("widen(dt, in_dtype, row * H + h)", "widen(dt, in_dtype, row * H)"),
+    "ssd_gate_offset": ("row * H * P + (int64_t)h * P + p);\n                out", "row * H * P + p);\n                out"),
+    "ssd_state_in_ignored": ("S[e] = ssm_state_in ? ssm_state_in[((int64_t)b * H + h) * P * N + e] : 0.0;",
+                             "S[e] = 0.0;"),
+    "ssd_conv_state_in_ignored": ("hist[c * (W - 1) + k] = conv_state_in ? conv_state_in[((int64_t)b * (W - 1) + k) * Cx + ch[c]] : 0.0;",
+                                  "hist[c * (W - 1) + k] = 0.0;"),
+    "ssd_conv_history_stores_u": ("if (W > 1) hist[c * (W - 1) + W - 2] = xt;", "if (W > 1) hist[c * (W - 1) + W - 2] = u[c];"),
+    "ssd_state_transposed": ("S[(int64_t)p * N + n] = a * S[(int64_t)p * N + n] + delta",
+                             "S[(int64_t)p * N + n] = a * S[(int64_t)n * P + p] + delta"),
 }
 
 
