@@ -317,6 +317,99 @@ int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype,
                        float* scales_out, void* cuda_stream);
 
 /*
+ * The SSD (Mamba-2-style) variant of the mixer.  The pages name the model families the
+ * mixer serves (Overview: Mamba, Falcon-Mamba, Zamba) but print no equations for this
+ * form; it follows the published Mamba-2 layer (Dao and Gu, "Transformers are SSMs",
+ * 2024).  Per batch row b, head h of H, group g = h / (H / G), position p < 64 and
+ * state n < 64:
+ *   [x | B | C]_t = SiLU(conv_b + causal width-4 depthwise conv of the raw xBC channels)
+ *   delta_t       = softplus(dt_t[h] + dt_bias[h])
+ *   S_t[p][n]     = exp(delta_t A[h]) S_{t-1}[p][n] + delta_t x_t[h][p] B_t[g][n]
+ *   out_t[h][p]   = (sum_n C_t[g][n] S_t[p][n] + D[h] x_t[h][p]) * SiLU(z_t[h][p])
+ * The recurrence stays inside its head (Methodology 2) and the final states are the
+ * cache that decode continues from (Methodology 3).
+ *
+ * Shapes (elements; channel stride 1):
+ *   xBC      [batch][L][Cx], Cx = 64 H + 128 G: channel 64 h + p is x of head h,
+ *            64 H + 64 g + n is B of group g, 64 H + 64 G + 64 g + n is C of group g
+ *   z        [batch][L][64 H]          dt  [batch][L][H]
+ *   conv_w   [Cx][4] (tap 3 multiplies the current token), conv_b [Cx]
+ *   A, Dskip, dt_bias  [H]             (float32)
+ *   conv_state [batch or slot][3][Cx]  the last three raw xBC inputs, oldest first (float32)
+ *   ssm_state  [batch or slot][H][64][64]  (float32)
+ * Supported: head_dim == 64, d_state == 64, d_conv == 4, H % G == 0.  Anything else
+ * returns SSM_ERR_UNSUPPORTED.
+ */
+
+/* Bytes of device workspace ssd_prefill needs for these sizes (0 on a bad size). */
+size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_groups);
+
+/*
+ * ssd_prefill -- the SSD mixer over L tokens, on the tensor cores.  The recurrence is
+ * computed chunk by chunk (128 tokens) in its matrix form: the products C B^T, M X, C S^T
+ * and the state update run as tcgen05 MMAs on bf16 hi + lo operand pairs with fp32
+ * accumulation, so every operand carries 16 significant bits.
+ *
+ *   batch, seqlen            1..65535 rows, 1..2^30 tokens
+ *   n_heads, head_dim        1..65535 heads of 64
+ *   n_groups, d_state        groups sharing B and C (n_heads % n_groups == 0), 64 states
+ *   d_conv                   4
+ *   in_dtype                 SSM_BF16 (xBC, z, dt); SSM_F32 returns SSM_ERR_UNSUPPORTED
+ *   out_dtype                SSM_F32 or SSM_BF16
+ *   xBC, xbc_stride_b/_t     view of [batch][L][Cx]: 16-byte aligned, strides multiples of 8,
+ *                            xbc_stride_t >= Cx
+ *   z, z_stride_b/_t         view of [batch][L][64 H]: same rules, z_stride_t >= 64 H
+ *   dt, dt_stride_b/_t       view of [batch][L][H]: element aligned, dt_stride_t >= H
+ *   conv_w (16-byte aligned), conv_b, A, Dskip, dt_bias
+ *   conv_state_in, ssm_state_in   NULL (zeros) or [batch][3][Cx] / [batch][H][64][64],
+ *                            contiguous; ssm_state_in 16-byte aligned
+ *   out, out_stride_b/_t     view of [batch][L][64 H] in out_dtype: 16-byte aligned, strides
+ *                            multiples of 16 bytes; rows may not overlap
+ *   conv_state_out, ssm_state_out  [batch][3][Cx] / [batch][H][64][64] float32, contiguous;
+ *                            ssm_state_out 16-byte aligned
+ *   workspace, workspace_bytes     device memory of at least
+ *                            ssd_prefill_workspace_bytes(batch, seqlen, n_groups) bytes,
+ *                            16-byte aligned, owned by the caller and not read afterwards
+ * Asynchronous on cuda_stream (two kernels).  Returns SSM_OK or a negative status.
+ */
+int ssd_prefill(int batch, int seqlen, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
+                ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                const void* xBC, int64_t xbc_stride_b, int64_t xbc_stride_t,
+                const void* z, int64_t z_stride_b, int64_t z_stride_t,
+                const void* dt, int64_t dt_stride_b, int64_t dt_stride_t,
+                const float* conv_w, const float* conv_b,
+                const float* A, const float* Dskip, const float* dt_bias,
+                const float* conv_state_in, const float* ssm_state_in,
+                void* out, int64_t out_stride_b, int64_t out_stride_t,
+                float* conv_state_out, float* ssm_state_out,
+                void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * ssd_decode_step -- one token per request of the SSD mixer, continuing from the cached
+ * states of its slot and updating them in place (Methodology 3).
+ *
+ *   batch                    1..65535 requests
+ *   n_heads .. d_conv        as for ssd_prefill
+ *   in_dtype, out_dtype      SSM_F32 or SSM_BF16
+ *   xBC, z, dt               [batch][Cx], [batch][64 H], [batch][H], contiguous, element aligned
+ *   conv_w (16-byte aligned), conv_b, A, Dskip, dt_bias   as for ssd_prefill
+ *   conv_state, ssm_state    [n_slots][3][Cx] / [n_slots][H][64][64] float32, in/out;
+ *                            ssm_state 16-byte aligned
+ *   n_slots, state_slot      request r uses slot state_slot[r] (NULL: slot r, then
+ *                            n_slots >= batch); a slot outside [0, n_slots) is skipped and
+ *                            sets SSM_DEV_BAD_SLOT; slots must be distinct
+ *   out                      [batch][64 H] in out_dtype, contiguous
+ * Asynchronous on cuda_stream (two kernels).  Returns SSM_OK or a negative status.
+ */
+int ssd_decode_step(int batch, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
+                    ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                    const void* xBC, const void* z, const void* dt,
+                    const float* conv_w, const float* conv_b,
+                    const float* A, const float* Dskip, const float* dt_bias,
+                    float* conv_state, float* ssm_state, int n_slots, const int32_t* state_slot,
+                    void* out, void* cuda_stream);
+
+/*
  * ssm_selftest_expire_wait -- a diagnostic with no counterpart in the pages: launches one
  * kernel that waits, through the library's bounded mbarrier wait, for a phase that nothing
  * completes.  After limit_us microseconds (1 .. 2e6) the wait gives up, the kernel sets

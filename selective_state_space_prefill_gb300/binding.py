@@ -22,7 +22,8 @@ DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
 
 EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_segmented",
            "ssm_prefill_segmented_noalloc", "ssm_decode_step", "ssm_decode_tokens", "ssm_out_proj_partial",
-           "q8_reduce_partials", "ssm_selftest_expire_wait", "ssm_device_status", "ssm_last_error")
+           "q8_reduce_partials", "ssd_prefill_workspace_bytes", "ssd_prefill", "ssd_decode_step",
+           "ssm_selftest_expire_wait", "ssm_device_status", "ssm_last_error")
 NOALLOC_SCRATCH_BYTES = 4 << 20     # SSM_NOALLOC_SCRATCH_BYTES
 
 
@@ -69,6 +70,13 @@ def load(path: Path | str | None = None):
     lib.ssm_out_proj_partial.restype = I
     lib.q8_reduce_partials.argtypes = [I, P, I, L, I, P, I, P, P, P]
     lib.q8_reduce_partials.restype = I
+    lib.ssd_prefill_workspace_bytes.argtypes = [I, I, I]
+    lib.ssd_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_prefill.argtypes = [I, I, I, I, I, I, I, I, I, P, L, L, P, L, L, P, L, L, P, P, P, P, P, P, P,
+                                P, L, L, P, P, P, ctypes.c_size_t, P]
+    lib.ssd_prefill.restype = I
+    lib.ssd_decode_step.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, I, P, P, P]
+    lib.ssd_decode_step.restype = I
     lib.ssm_selftest_expire_wait.argtypes = [I, P]
     lib.ssm_selftest_expire_wait.restype = I
     lib.ssm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
@@ -365,3 +373,109 @@ def selftest_expire_wait(limit_us: int = 50000, stream=None) -> None:
     """ssm_selftest_expire_wait: one kernel whose bounded wait expires after limit_us."""
     lib = load()
     _check(lib, "ssm_selftest_expire_wait", lib.ssm_selftest_expire_wait(int(limit_us), _stream(stream)))
+
+
+# ------------------------------------------------------------------ SSD (Mamba-2-style) mixer
+def _ssd_dims(n_heads, n_groups, head_dim=64, d_state=64):
+    return n_heads * head_dim, n_heads * head_dim + 2 * n_groups * d_state
+
+
+def ssd_prefill_workspace_bytes(batch: int, seqlen: int, n_groups: int) -> int:
+    """ssd_prefill_workspace_bytes: device bytes ssd_prefill needs."""
+    return int(load().ssd_prefill_workspace_bytes(batch, seqlen, n_groups))
+
+
+def _ssd_params(conv_w, conv_b, A, D, dt_bias, H, Cx):
+    _param(conv_w, (Cx, 4), "conv_w")
+    _param(conv_b, (Cx,), "conv_b")
+    for t, n in ((A, "A"), (D, "D"), (dt_bias, "dt_bias")):
+        _param(t, (H,), n)
+
+
+def _ssd_states(t, batch, H, Cx, name, conv):
+    shape = (batch, 3, Cx) if conv else (batch, H, 64, 64)
+    if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous float32 {shape}")
+
+
+def ssd_prefill(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, n_heads, n_groups, conv_state_in=None,
+                ssm_state_in=None, out=None, out_dtype=torch.float32, conv_state_out=None, ssm_state_out=None,
+                workspace=None, stream=None):
+    """ssd_prefill: xBC [batch, L, 64 H + 128 G], z [batch, L, 64 H], dt [batch, L, H] bf16
+    (channel-stride-1 views), head_dim = d_state = 64.  ``workspace`` (a CUDA uint8 tensor of at
+    least ssd_prefill_workspace_bytes(...) bytes) is allocated here with torch when not given.
+    Returns (out [batch, L, 64 H], conv_state_out [batch, 3, Cx], ssm_state_out [batch, H, 64, 64])."""
+    lib = load()
+    _need_cuda(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, conv_state_in, ssm_state_in)
+    H, G = int(n_heads), int(n_groups)
+    HP, Cx = _ssd_dims(H, G)
+    batch, L, cx = xBC.shape
+    if cx != Cx or tuple(z.shape) != (batch, L, HP) or tuple(dt.shape) != (batch, L, H):
+        raise ValueError("xBC, z, dt shapes disagree with n_heads / n_groups")
+    if z.dtype != xBC.dtype or dt.dtype != xBC.dtype:
+        raise ValueError("xBC, z, dt must share one dtype")
+    for t, n in ((xBC, "xBC"), (z, "z"), (dt, "dt")):
+        _chan_contig(t, n)
+    _ssd_params(conv_w, conv_b, A, D, dt_bias, H, Cx)
+    dev = xBC.device
+    if out is None:
+        out = torch.empty(batch, L, HP, device=dev, dtype=out_dtype)
+    _chan_contig(out, "out")
+    if conv_state_out is None:
+        conv_state_out = torch.empty(batch, 3, Cx, device=dev, dtype=torch.float32)
+    if ssm_state_out is None:
+        ssm_state_out = torch.empty(batch, H, 64, 64, device=dev, dtype=torch.float32)
+    for t, n, c in ((conv_state_out, "conv_state_out", True), (ssm_state_out, "ssm_state_out", False),
+                    (conv_state_in, "conv_state_in", True), (ssm_state_in, "ssm_state_in", False)):
+        if t is not None:
+            _ssd_states(t, batch, H, Cx, n, c)
+    need = int(lib.ssd_prefill_workspace_bytes(batch, L, G))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
+    _need_cuda(workspace)
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    rc = lib.ssd_prefill(batch, L, H, 64, G, 64, 4, _dtype_code(xBC.dtype), _dtype_code(out.dtype),
+                         _ptr(xBC), xBC.stride(0), xBC.stride(1), _ptr(z), z.stride(0), z.stride(1),
+                         _ptr(dt), dt.stride(0), dt.stride(1), _ptr(conv_w), _ptr(conv_b), _ptr(A), _ptr(D),
+                         _ptr(dt_bias), _ptr(conv_state_in), _ptr(ssm_state_in), _ptr(out), out.stride(0),
+                         out.stride(1), _ptr(conv_state_out), _ptr(ssm_state_out), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(lib, "ssd_prefill", rc)
+    return out, conv_state_out, ssm_state_out
+
+
+def ssd_decode_step(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, n_heads, n_groups, conv_state, ssm_state,
+                    state_slot=None, out=None, out_dtype=torch.float32, stream=None):
+    """ssd_decode_step: xBC [batch, Cx], z [batch, 64 H], dt [batch, H] (contiguous); the cached
+    states conv_state [n_slots, 3, Cx] and ssm_state [n_slots, H, 64, 64] advance one token in
+    place.  Returns out [batch, 64 H]."""
+    lib = load()
+    _need_cuda(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, conv_state, ssm_state, state_slot)
+    H, G = int(n_heads), int(n_groups)
+    HP, Cx = _ssd_dims(H, G)
+    batch = xBC.shape[0]
+    if tuple(xBC.shape) != (batch, Cx) or tuple(z.shape) != (batch, HP) or tuple(dt.shape) != (batch, H):
+        raise ValueError("xBC, z, dt shapes disagree with n_heads / n_groups")
+    if z.dtype != xBC.dtype or dt.dtype != xBC.dtype:
+        raise ValueError("xBC, z, dt must share one dtype")
+    for t, n in ((xBC, "xBC"), (z, "z"), (dt, "dt")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _ssd_params(conv_w, conv_b, A, D, dt_bias, H, Cx)
+    n_slots = conv_state.shape[0]
+    _ssd_states(conv_state, n_slots, H, Cx, "conv_state", True)
+    _ssd_states(ssm_state, n_slots, H, Cx, "ssm_state", False)
+    if state_slot is not None and (state_slot.dtype != torch.int32 or tuple(state_slot.shape) != (batch,)
+                                   or not state_slot.is_contiguous()):
+        raise ValueError("state_slot must be contiguous int32 [batch]")
+    if out is None:
+        out = torch.empty(batch, HP, device=xBC.device, dtype=out_dtype)
+    if not out.is_contiguous() or tuple(out.shape) != (batch, HP):
+        raise ValueError("out must be contiguous [batch, 64 H]")
+    rc = lib.ssd_decode_step(batch, H, 64, G, 64, 4, _dtype_code(xBC.dtype), _dtype_code(out.dtype),
+                             _ptr(xBC), _ptr(z), _ptr(dt), _ptr(conv_w), _ptr(conv_b), _ptr(A), _ptr(D),
+                             _ptr(dt_bias), _ptr(conv_state), _ptr(ssm_state), n_slots, _ptr(state_slot),
+                             _ptr(out), _stream(stream))
+    _check(lib, "ssd_decode_step", rc)
+    return out

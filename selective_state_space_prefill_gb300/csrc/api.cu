@@ -3,7 +3,8 @@
 // Every entry point validates its arguments on the host, returns a negative
 // status (with a message for ssm_last_error) before launching anything when they
 // are wrong, and otherwise enqueues its kernels on the caller's stream (one
-// kernel; three for a prefill cut into several sequence segments).
+// kernel; three for a prefill cut into several sequence segments; two for the
+// SSD prefill and decode).
 // No entry point allocates memory or keeps per-call state.
 #include <stdarg.h>
 #include <stdio.h>
@@ -191,7 +192,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
 
 extern "C" {
 
-int ssm_abi_version(void) { return 104; }
+int ssm_abi_version(void) { return 105; }
 
 const char* ssm_last_error(void) { return g_err; }
 
@@ -286,6 +287,150 @@ int ssm_out_proj_partial(int64_t M, int64_t N, int64_t K, const void* y, int64_t
     a.status = status;
     const char* why = "";
     if (ssm::launch_out_proj(a, y, W, ldy, ldw, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
+    return SSM_OK;
+}
+
+size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_groups) {
+    if (batch < 1 || batch > 65535 || seqlen < 1 || seqlen > (1 << 30) || n_groups < 1 || n_groups > 65535) return 0;
+    return ssm::ssd_workspace_layout(batch, seqlen, n_groups).bytes;
+}
+
+int ssd_prefill(int batch, int seqlen, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
+                ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                const void* xBC, int64_t xbc_stride_b, int64_t xbc_stride_t,
+                const void* z, int64_t z_stride_b, int64_t z_stride_t,
+                const void* dt, int64_t dt_stride_b, int64_t dt_stride_t,
+                const float* conv_w, const float* conv_b,
+                const float* A, const float* Dskip, const float* dt_bias,
+                const float* conv_state_in, const float* ssm_state_in,
+                void* out, int64_t out_stride_b, int64_t out_stride_t,
+                float* conv_state_out, float* ssm_state_out,
+                void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    static const char* fn = "ssd_prefill";
+    g_err[0] = 0;
+    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: batch %d not in [1, 65535]", fn, batch);
+    if (seqlen < 1 || seqlen > (1 << 30)) return fail(SSM_ERR_INVALID_ARG, "%s: seqlen %d not in [1, 2^30]", fn, seqlen);
+    if (n_heads < 1 || n_heads > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: n_heads %d not in [1, 65535]", fn, n_heads);
+    if (n_groups < 1 || n_heads % n_groups != 0)
+        return fail(SSM_ERR_INVALID_ARG, "%s: n_groups %d does not divide n_heads %d", fn, n_groups, n_heads);
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (head_dim != 64 || d_state != 64 || d_conv != 4)
+        return fail(SSM_ERR_UNSUPPORTED, "%s: head_dim %d, d_state %d, d_conv %d unsupported (64, 64, 4 only)", fn,
+                    head_dim, d_state, d_conv);
+    if (in_dtype != SSM_BF16) return fail(SSM_ERR_UNSUPPORTED, "%s: token inputs must be bf16", fn);
+    if (!xBC || !z || !dt || !conv_w || !conv_b || !A || !Dskip || !dt_bias || !out || !conv_state_out ||
+        !ssm_state_out || !workspace)
+        return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    const int64_t HP = 64LL * n_heads, Cx = HP + 128LL * n_groups;
+    if (xbc_stride_t < Cx || z_stride_t < HP || dt_stride_t < n_heads || out_stride_t < HP)
+        return fail(SSM_ERR_INVALID_ARG, "%s: a token stride is below the row width", fn);
+    if (batch > 1 && (xbc_stride_b < (int64_t)(seqlen - 1) * xbc_stride_t + Cx ||
+                      z_stride_b < (int64_t)(seqlen - 1) * z_stride_t + HP ||
+                      dt_stride_b < (int64_t)(seqlen - 1) * dt_stride_t + n_heads))
+        return fail(SSM_ERR_INVALID_ARG, "%s: a batch stride lets rows overlap", fn);
+    if (batch > 1 && out_stride_b < (int64_t)(seqlen - 1) * out_stride_t + HP)
+        return fail(SSM_ERR_INVALID_ARG, "%s: out_stride_b %lld lets batch rows overlap", fn, (long long)out_stride_b);
+    const size_t need = ssm::ssd_workspace_layout(batch, seqlen, n_groups).bytes;
+    if (workspace_bytes < need)
+        return fail(SSM_ERR_INVALID_ARG, "%s: workspace of %zu bytes given, %zu needed", fn, workspace_bytes, need);
+    const int oe = esize(out_dtype);
+    if (!aligned(xBC, 16) || !aligned(z, 16) || xbc_stride_t % 8 || xbc_stride_b % 8 || z_stride_t % 8 || z_stride_b % 8)
+        return fail(SSM_ERR_MISALIGNED, "%s: xBC and z must be 16-byte aligned with strides of 16 bytes", fn);
+    if (!aligned(out, 16) || (out_stride_t * oe) % 16 || (out_stride_b * oe) % 16)
+        return fail(SSM_ERR_MISALIGNED, "%s: out must be 16-byte aligned with strides of 16 bytes", fn);
+    if (!aligned(conv_w, 16) || !aligned(ssm_state_out, 16) || (ssm_state_in && !aligned(ssm_state_in, 16)) ||
+        !aligned(workspace, 16) || !aligned(dt, 2))
+        return fail(SSM_ERR_MISALIGNED, "%s: conv_w, the ssm states and the workspace need 16-byte alignment", fn);
+
+    int serr = 0;
+    unsigned int* status = status_ptr(&serr);
+    if (serr) return fail(SSM_ERR_CUDA, "%s: no usable CUDA device", fn);
+    ssm::SsdArgs a{};
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.n_heads = n_heads;
+    a.n_groups = n_groups;
+    a.xBC = xBC;
+    a.xbc_stride_b = xbc_stride_b;
+    a.xbc_stride_t = xbc_stride_t;
+    a.z = z;
+    a.z_stride_b = z_stride_b;
+    a.z_stride_t = z_stride_t;
+    a.dt = dt;
+    a.dt_stride_b = dt_stride_b;
+    a.dt_stride_t = dt_stride_t;
+    a.conv_w = conv_w;
+    a.conv_b = conv_b;
+    a.A = A;
+    a.Dskip = Dskip;
+    a.dt_bias = dt_bias;
+    a.conv_state_in = conv_state_in;
+    a.ssm_state_in = ssm_state_in;
+    a.out = out;
+    a.out_stride_b = out_stride_b;
+    a.out_stride_t = out_stride_t;
+    a.conv_state_out = conv_state_out;
+    a.ssm_state_out = ssm_state_out;
+    a.workspace = workspace;
+    a.status = status;
+    const char* why = "";
+    if (ssm::launch_ssd_prefill(a, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
+    return SSM_OK;
+}
+
+int ssd_decode_step(int batch, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
+                    ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                    const void* xBC, const void* z, const void* dt,
+                    const float* conv_w, const float* conv_b,
+                    const float* A, const float* Dskip, const float* dt_bias,
+                    float* conv_state, float* ssm_state, int n_slots, const int32_t* state_slot,
+                    void* out, void* cuda_stream) {
+    static const char* fn = "ssd_decode_step";
+    g_err[0] = 0;
+    if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: batch %d not in [1, 65535]", fn, batch);
+    if (n_heads < 1 || n_heads > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: n_heads %d not in [1, 65535]", fn, n_heads);
+    if (n_groups < 1 || n_heads % n_groups != 0)
+        return fail(SSM_ERR_INVALID_ARG, "%s: n_groups %d does not divide n_heads %d", fn, n_groups, n_heads);
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (head_dim != 64 || d_state != 64 || d_conv != 4)
+        return fail(SSM_ERR_UNSUPPORTED, "%s: head_dim %d, d_state %d, d_conv %d unsupported (64, 64, 4 only)", fn,
+                    head_dim, d_state, d_conv);
+    if (!xBC || !z || !dt || !conv_w || !conv_b || !A || !Dskip || !dt_bias || !conv_state || !ssm_state || !out)
+        return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (n_slots < 1 || (!state_slot && n_slots < batch))
+        return fail(SSM_ERR_INVALID_ARG, "%s: n_slots %d too small", fn, n_slots);
+    const int es = esize(in_dtype);
+    if (!aligned(conv_w, 16) || !aligned(ssm_state, 16))
+        return fail(SSM_ERR_MISALIGNED, "%s: conv_w and ssm_state need 16-byte alignment", fn);
+    if (!aligned(xBC, es) || !aligned(z, es) || !aligned(dt, es) || !aligned(out, esize(out_dtype)) ||
+        !aligned(conv_state, 4) || (state_slot && !aligned(state_slot, 4)))
+        return fail(SSM_ERR_MISALIGNED, "%s: a pointer is not element aligned", fn);
+    int serr = 0;
+    unsigned int* status = status_ptr(&serr);
+    if (serr) return fail(SSM_ERR_CUDA, "%s: no usable CUDA device", fn);
+    ssm::SsdDecodeArgs a{};
+    a.batch = batch;
+    a.n_heads = n_heads;
+    a.n_groups = n_groups;
+    a.n_slots = n_slots;
+    a.xBC = xBC;
+    a.z = z;
+    a.dt = dt;
+    a.conv_w = conv_w;
+    a.conv_b = conv_b;
+    a.A = A;
+    a.Dskip = Dskip;
+    a.dt_bias = dt_bias;
+    a.conv_state = conv_state;
+    a.ssm_state = ssm_state;
+    a.state_slot = state_slot;
+    a.out = out;
+    a.status = status;
+    const char* why = "";
+    if (ssm::launch_ssd_decode(a, in_dtype == SSM_BF16, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream),
+                               &why) != 0)
         return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
     return SSM_OK;
 }

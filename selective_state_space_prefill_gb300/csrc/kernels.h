@@ -72,7 +72,51 @@ struct OutProjArgs {
     unsigned int* status;
 };
 
+// SSD (Mamba-2-style) mixer: head dim 64, d_state 64, conv width 4, bf16 token inputs.
+//   xBC [batch][L][H*64 + 2*G*64] (x of every head, then B and C of every group), z [batch][L][H*64],
+//   dt [batch][L][H]; strides in elements; conv_state [batch][3][Cx], ssm_state [batch][H][64][64].
+struct SsdArgs {
+    int batch, seqlen, n_heads, n_groups;
+    const void* xBC;
+    int64_t xbc_stride_b, xbc_stride_t;
+    const void* z;
+    int64_t z_stride_b, z_stride_t;
+    const void* dt;
+    int64_t dt_stride_b, dt_stride_t;
+    const float *conv_w, *conv_b, *A, *Dskip, *dt_bias;
+    const float *conv_state_in, *ssm_state_in;
+    void* out;
+    int64_t out_stride_b, out_stride_t;
+    float *conv_state_out, *ssm_state_out;
+    void* workspace;                // B and C of every group after conv + SiLU, as bf16 hi/lo planes
+    int64_t ws_bt_off, ws_lp;       // filled in by launch_ssd_prefill
+    unsigned int* status;
+};
+
+// Workspace of an SSD prefill: 4 planes [batch*G][L][64] (C hi, C lo, B hi, B lo), then at
+// bt_off 2 planes [batch*G][64][lp] (B hi, B lo, token-major), lp = L rounded up to 128.
+struct SsdWorkspace {
+    size_t bytes;
+    int64_t bt_off, lp;
+};
+SsdWorkspace ssd_workspace_layout(int batch, int seqlen, int n_groups);
+
+// One-token SSD decode for a batch of requests, in place on the cached states of their slots.
+//   xBC [batch][Cx], z [batch][H*64], dt [batch][H] contiguous; conv_state [n_slots][3][Cx],
+//   ssm_state [n_slots][H][64][64]; out [batch][H*64].
+struct SsdDecodeArgs {
+    int batch, n_heads, n_groups, n_slots;
+    const void *xBC, *z, *dt;
+    const float *conv_w, *conv_b, *A, *Dskip, *dt_bias;
+    float *conv_state, *ssm_state;
+    const int32_t* state_slot;
+    void* out;
+    unsigned int* status;
+};
+
 // Each returns 0 on success, or -1 with *why set to a static message.
+int launch_ssd_prefill(const SsdArgs& a, bool out_bf16, cudaStream_t stream, const char** why);
+int launch_ssd_decode(const SsdDecodeArgs& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
 int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why);
 int launch_decode(const DecodeArgs& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
 int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding.EXPORTS)
     for fn in names:
         assert hasattr(lib, fn), fn
-    assert lib.ssm_abi_version() == 104
+    assert lib.ssm_abi_version() == 105
 
 
 FAKE = 0x10000  # 64 KiB-aligned fake device address, never dereferenced
@@ -197,3 +197,59 @@ def test_out_proj_rejects_bad_arguments(lib, kw, code):
 @pytest.mark.parametrize("limit", [0, -5, 2000001])
 def test_selftest_rejects_bad_limits(lib, limit):
     assert lib.ssm_selftest_expire_wait(limit, None) == INVALID
+
+
+def _ssd(lib, ws_bytes=1 << 30, **kw):
+    H, G, L = 4, 1, 300
+    Cx = 64 * H + 128 * G
+    a = dict(batch=2, seqlen=L, H=H, P=64, G=G, N=64, W=4, in_dtype=1, out_dtype=0,
+             xBC=FAKE, xsb=L * Cx, xst=Cx, z=FAKE, zsb=L * 64 * H, zst=64 * H, dt=FAKE, dsb=L * H, dst=H,
+             conv_w=FAKE, conv_b=FAKE, A=FAKE, D=FAKE, dt_bias=FAKE, csi=None, ssi=None,
+             out=FAKE, osb=L * 64 * H, ost=64 * H, cso=FAKE, sso=FAKE, ws=FAKE)
+    a.update(kw)
+    return lib.ssd_prefill(*a.values(), ws_bytes, None)
+
+
+def test_ssd_workspace_bytes(lib):
+    # 4 planes [B*G][L][64] + 2 planes [B*G][64][L rounded up to 128], bf16
+    assert lib.ssd_prefill_workspace_bytes(4, 2048, 1) == 4 * 4 * 2048 * 64 * 2 + 2 * 4 * 64 * 2048 * 2
+    assert lib.ssd_prefill_workspace_bytes(1, 300, 2) == 4 * 2 * 300 * 128 + 2 * 2 * 64 * 384 * 2
+    assert lib.ssd_prefill_workspace_bytes(0, 300, 2) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=0), INVALID), (dict(seqlen=0), INVALID), (dict(H=0), INVALID), (dict(G=3), INVALID),
+    (dict(P=32), UNSUPPORTED), (dict(N=128), UNSUPPORTED), (dict(W=3), UNSUPPORTED), (dict(in_dtype=0), UNSUPPORTED),
+    (dict(out_dtype=4), INVALID), (dict(xBC=None), INVALID), (dict(ws=None), INVALID), (dict(xst=100), INVALID),
+    (dict(ost=64), INVALID), (dict(dsb=3), INVALID), (dict(ws_bytes=1000), INVALID), (dict(xBC=FAKE + 8), MISALIGNED),
+    (dict(xst=388, xsb=300 * 388), MISALIGNED), (dict(out=FAKE + 4), MISALIGNED), (dict(sso=FAKE + 8), MISALIGNED),
+    (dict(ws=FAKE + 8), MISALIGNED),
+])
+def test_ssd_prefill_rejects_bad_arguments(lib, kw, code):
+    assert _ssd(lib, **kw) == code
+    assert lib.ssm_last_error().decode().startswith("ssd_prefill")
+
+
+def _ssd_dec(lib, **kw):
+    a = dict(batch=2, H=4, P=64, G=2, N=64, W=4, in_dtype=1, out_dtype=0, xBC=FAKE, z=FAKE, dt=FAKE,
+             conv_w=FAKE, conv_b=FAKE, A=FAKE, D=FAKE, dt_bias=FAKE, cs=FAKE, ss=FAKE, n_slots=2, slot=None,
+             out=FAKE, stream=None)
+    a.update(kw)
+    return lib.ssd_decode_step(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=0), INVALID), (dict(G=3), INVALID), (dict(N=16), UNSUPPORTED), (dict(cs=None), INVALID),
+    (dict(n_slots=1), INVALID), (dict(ss=FAKE + 4), MISALIGNED), (dict(xBC=FAKE + 1), MISALIGNED),
+])
+def test_ssd_decode_rejects_bad_arguments(lib, kw, code):
+    assert _ssd_dec(lib, **kw) == code
+    assert lib.ssm_last_error().decode().startswith("ssd_decode_step")
+
+
+def test_ssd_valid_call_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _ssd(lib) == CUDA
+    assert _ssd_dec(lib) == CUDA
