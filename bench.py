@@ -747,8 +747,9 @@ def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4, graph_calls=64):
 def run_profile_target(which: str):
     """Launch one kernel 4 times (3 warm-up + 1 to capture) for ncu: the prefill on the bench
     workload, the segmented prefill of a batch-1 row, the decode step at batch 256 x d_inner
-    8192, q8 over P=4 bf16 [4096, 1, 4096], or the out_proj partial of the Falcon-Mamba-like
-    rank (16384 x 4096 x 2048)."""
+    8192, q8 over P=4 bf16 [4096, 1, 4096], the out_proj partial of the Falcon-Mamba-like
+    rank (16384 x 4096 x 2048), or the SSD prefill of the Zamba2-2.7B-like layer (4 x 2048
+    tokens, 80 heads of 64, d_state 64, one group)."""
     import torch
     from selective_state_space_prefill_gb300 import build as ssm_build
     if not ssm_build.up_to_date():
@@ -779,6 +780,14 @@ def run_profile_target(which: str):
         for _ in range(4):
             ssm.decode_step(tok["x"], tok["z"], tok["dt"], tok["B"], tok["C"], par["A"], par["D"],
                             par["dt_bias"], par["conv_w"], par["conv_b"], cs, ss, out=out)
+    elif which == "ssd":
+        from selective_state_space_prefill_gb300.inputs import make_ssd_inputs
+        B, L, H, G = 4, 2048, 80, 1
+        inp = make_ssd_inputs(B, L, H, n_groups=G, seed=0, device=dev)
+        ws = torch.empty(ssm.ssd_prefill_workspace_bytes(B, L, G), device=dev, dtype=torch.uint8)
+        for _ in range(4):
+            ssm.ssd_prefill(inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G,
+                            workspace=ws)
     elif which == "out_proj":
         from selective_state_space_prefill_gb300.inputs import make_out_proj_inputs
         y, W = make_out_proj_inputs(16384, 2048, 4096, seed=0, device=dev)
@@ -804,7 +813,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8", "out_proj"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8", "out_proj", "ssd"], default=None,
                     help="only launch one kernel 4 times (for an ncu capture) and exit")
     args = ap.parse_args()
     _set_workload(args.workload)

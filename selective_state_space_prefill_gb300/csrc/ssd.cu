@@ -14,8 +14,8 @@
 // The decay is a scalar per head, so inside a chunk of Q = 128 tokens the recurrence is a
 // sequence of dense contractions (the SSD "dual" form).  With s_i = sum_{r<=i} delta_r A[h]:
 //   G = C B^T                                   [Q x Q]
-//   M[i][j] = G[i][j] exp(s_i - s_j) delta_j    (j <= i, else 0)
-//   Y = M X + exp(s)_i (C S_prev^T) + D X        (X = the chunk's x, [Q x 64])
+//   M[i][j] = G[i][j] exp(s_i - s_j) delta_j    (j < i, else 0),  M[i][i] = G[i][i] delta_i + D
+//   Y = M X + exp(s)_i (C S_prev^T)              (X = the chunk's x, [Q x 64]; D x rides on M's diagonal)
 //   S = exp(s_Q) S_prev + sum_j exp(s_Q - s_j) delta_j x_j (x) B_j
 // Those four products run on the 5th-generation tensor cores (tcgen05, kind::f16, M = 128,
 // fp32 accumulators in TMEM).  bf16 operands alone would round x, B, C, M and S by 2^-9 each,
@@ -49,7 +49,11 @@ using Tin_bf16 = __nv_bfloat16;  // the prefill's token inputs (x, B, C, z, dt) 
 constexpr int kQ = 128;        // tokens per chunk (the MMA's M)
 constexpr int kP = 64;         // head dim
 constexpr int kNs = 64;        // d_state
-constexpr int kTh = 256;       // threads of k_ssd_chunk: warp w reads TMEM lanes 32 (w % 4).., column half w / 4
+constexpr int kTh = 512;       // threads of k_ssd_chunk: warp w reads TMEM lanes 32 (w % 4) .. + 31
+constexpr int kWG = kTh / 128; // column groups: warp w works on column group w / 4 of its rows
+constexpr int kCW = kP / kWG;  // columns of x, y, S per thread (16)
+constexpr int kMJ = kQ / kWG;  // columns of M per thread (32)
+static_assert(kCW % 8 == 0 && kMJ % 32 == 0, "column split");
 
 // tcgen05.mma kind::f16 instruction descriptors: fp32 accumulator, bf16 A and B, both K-major,
 // M = 128, N = 128 or 64.
@@ -67,20 +71,19 @@ struct Smem {
     static constexpr int XW = 131072;                // weighted X^T, hi rows 0-63 / lo rows 64-127,
                                                      // r0 and r1 [128][64 t] each; later fp32 scratch
     static constexpr int SHI = 163840, SLO = 172032; // S hi / lo [64 p][64 n]
-    static constexpr int XR = 180224;                // raw x [131 t][64 p] bf16 (TMA, unswizzled)
-    static constexpr int ZT = 197632;                // z [128 t][64 p] bf16 (TMA, unswizzled)
-    static constexpr int DL = 214016;                // delta [128] f32
-    static constexpr int CS = DL + 512;              // s (chunk-local cumulative delta*A) [128] f32
-    static constexpr int CW = CS + 512;              // conv weights of the head's x channels [64][4]
+    static constexpr int XR = 180224;                // raw x [131 t][64 p] bf16 (TMA, 128-byte swizzle)
+    static constexpr int ZT = 197632;                // z [128 t][64 p] bf16 (TMA, 128-byte swizzle)
+    static constexpr int DL = 214016;                // delta [2][128] f32 (by chunk parity)
+    static constexpr int CS = DL + 1024;             // s (chunk-local cumulative delta*A) [2][128] f32
+    static constexpr int CW = CS + 1024;             // conv weights of the head's x channels [64][4]
     static constexpr int CB = CW + 1024;             // conv bias [64]
     static constexpr int WS = CB + 256;              // per-warp scan totals [4]
-    static constexpr int BAR = WS + 64;              // bar_a, bar_b, bar_mma
-    static constexpr int SLOT = BAR + 32;            // TMEM base address
+    static constexpr int BAR = WS + 64;              // nine mbarriers (TMA, MMA groups, hand-offs)
+    static constexpr int SLOT = BAR + 80;            // TMEM base address, error flag
     static constexpr int TOTAL = SLOT + 16;
     static constexpr int ALLOC = TOTAL + 1024;       // + slack to align the base to 1024
     static constexpr int XR_BYTES = (kQ + 3) * kP * 2;
     static constexpr int TX_A = XR_BYTES + 4 * 8192;     // raw x + B^T hi/lo
-    static constexpr int TX_B = 4 * 16384 + kQ * kP * 2; // C hi/lo, B hi/lo + z
     static constexpr int SCR_LD = 68;                    // fp32 scratch row stride (floats)
 };
 static_assert(Smem::XR + Smem::XR_BYTES <= Smem::ZT, "raw x tile overlaps z");
@@ -101,15 +104,12 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
-__device__ __forceinline__ void st_u16(unsigned char* base, uint32_t off, __nv_bfloat16 v) {
-    *reinterpret_cast<__nv_bfloat16*>(base + off) = v;
-}
-
 // Four K-steps (K = 64) of D (+)= A B^T for K-major operands at shared addresses a, b.
+// The descriptor's address field counts 16-byte units, so a 32-byte K-step adds 2 to it.
 __device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool first) {
+    const uint64_t da = smem_desc_sw128(a), db = smem_desc_sw128(b);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(d, smem_desc_sw128(a + 32 * kk), smem_desc_sw128(b + 32 * kk), idesc, (first && kk == 0) ? 0u : 1u);
+    for (int kk = 0; kk < 4; ++kk) mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
 }
 
 // ------------------------------------------------------------------ pre-pass: B and C
@@ -165,27 +165,61 @@ k_ssd_bc(const SsdArgs p) {
 }
 
 // ------------------------------------------------------------------ prefill chunks
+// Warps 0-15 ("workers") own the arithmetic on the threads; warp 16 ("producer", one elected
+// lane) issues every TMA copy and tcgen05.mma.  A chunk runs in phases; the tensor cores work on
+// one group of products while the workers work on the next:
+//   workers                                         producer
+//   2. (raw x) delta, s, conv + SiLU -> X^T, w x     1. (C, B tiles; previous chunk done)
+//      -> "X ready"                                     G = C B^T, Y_inter = C S_prev^T; z
+//   3. (G) M -> over the C, B tiles -> "M ready"     2. (X ready) dS^T = (w x)^T B
+//   4. (dS) S = 2^(s_Q) S + dS -> S tiles            3. (M ready) Y_intra = M X
+//   5. (Y_intra, z) out = (Y_intra + 2^(s_i) Y_inter) 4. (dS) refill raw x, B^T
+//      SiLU(z) -> "chunk done"                       5. (Y_intra) refill C, B
+// Each TMA group, MMA group and hand-off completes its own mbarrier once per chunk.  Every wait
+// is bounded; a worker whose wait expires keeps walking the chunk without waiting and the error
+// is OR-reduced at the next worker barrier, so no warp is ever left waiting at a barrier.
+constexpr int kWorkers = kTh;                        // 512 worker threads
+constexpr int kThAll = kTh + 32;                     // + the producer warp
+
+__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory"); }
+__device__ __forceinline__ bool workers_any(bool v) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)v), "n"(kWorkers) : "memory");
+    return r != 0;
+}
+
+// hi/lo bf16 pairs of two floats, packed as (lo element in the low half)
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 template <typename Tout>
-__global__ void __launch_bounds__(kTh, 1)
+__global__ void __launch_bounds__(kThAll, 1)
 k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
             const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ CUtensorMap tm_bt,
             const SsdArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float* s_dl = reinterpret_cast<float*>(sm + Smem::DL);
-    float* s_cs = reinterpret_cast<float*>(sm + Smem::CS);
     float* s_cw = reinterpret_cast<float*>(sm + Smem::CW);
     float* s_cb = reinterpret_cast<float*>(sm + Smem::CB);
     float* s_ws = reinterpret_cast<float*>(sm + Smem::WS);
-    uint64_t* bar_a = reinterpret_cast<uint64_t*>(sm + Smem::BAR);   // raw x + B^T of a chunk
-    uint64_t* bar_b = bar_a + 1;                                     // C, B tiles + z of a chunk
-    uint64_t* bar_m = bar_a + 2;                                     // MMA completion
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::BAR);
+    // TMA groups (raw x + B^T, C/B tiles, z), MMA groups (G + Y_inter, dS, Y_intra), hand-offs
+    enum { kBarA = 0, kBarB, kBarZ, kBarG, kBarD, kBarY, kXReady, kMReady, kDone, NBAR };
     uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Smem::SLOT);
+    int* s_err = reinterpret_cast<int*>(sm + Smem::SLOT + 4);
     const uint32_t sb = smem_u32(sm);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, hf = warp >> 2;
-    const int i = 32 * q + lane;                     // this thread's token row of the chunk
+    const bool producer = warp == kWorkers / 32;
+    const int q = warp & 3, cg = (warp >> 2) & (kWG - 1);
+    const int i = 32 * q + lane;                     // a worker's token row of the chunk
     const int h = blockIdx.x, b = blockIdx.y;
     const int H = p.n_heads, G = p.n_groups, L = p.seqlen;
     const int g = h / (H / G), BG = p.batch * G, bg = b * G + g;
@@ -195,9 +229,8 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const Tin_bf16* dtp = reinterpret_cast<const Tin_bf16*>(p.dt) + (int64_t)b * p.dt_stride_b + h;
 
     if (tid == 0) {
-        mbar_init(bar_a, 1);
-        mbar_init(bar_b, 1);
-        mbar_init(bar_m, 1);
+        for (int k = 0; k < NBAR; ++k) mbar_init(&bars[k], k >= kXReady ? kWorkers / 32 : 1);
+        *s_err = 0;
         fence_barrier_init();
         prefetch_tmap(&tm_x);
         prefetch_tmap(&tm_z);
@@ -213,38 +246,32 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         s_cw[4 * tid + 3] = w.w;
         s_cb[tid] = p.conv_b[h * (int64_t)kP + tid];
     }
-    // the state S[p][n] for p = i (q < 2), n in [32 hf, 32 hf + 32): fp32 in registers
-    float S[32];
+    // the state S[p][n] for p = i (workers with q < 2), n in [kCW cg, kCW cg + kCW): fp32 registers
+    float S[kCW];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) S[k] = 0.f;
-    if (q < 2 && p.ssm_state_in) {
+    for (int k = 0; k < kCW; ++k) S[k] = 0.f;
+    if (!producer && q < 2 && p.ssm_state_in) {
         const float4* src = reinterpret_cast<const float4*>(
-            p.ssm_state_in + (((int64_t)b * H + h) * kP + i) * kNs + 32 * hf);
+            p.ssm_state_in + (((int64_t)b * H + h) * kP + i) * kNs + kCW * cg);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kCW / 4; ++k) {
             const float4 v = src[k];
             S[4 * k] = v.x; S[4 * k + 1] = v.y; S[4 * k + 2] = v.z; S[4 * k + 3] = v.w;
         }
     }
-    // write S as the hi/lo operand tiles [p][n] the first chunk's C S^T reads
+    // S as the hi/lo operand tiles [p][n] that C S^T reads
     auto store_state = [&]() {
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
+        for (int c8 = 0; c8 < kCW / 8; ++c8) {
             uint32_t whi[4], wlo[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                __nv_bfloat16 h0, l0, h1, l1;
-                split_bf16(S[8 * c8 + 2 * k], h0, l0);
-                split_bf16(S[8 * c8 + 2 * k + 1], h1, l1);
-                whi[k] = pack2(h0, h1);
-                wlo[k] = pack2(l0, l1);
-            }
-            const uint32_t off = sw128(i, 32 * hf + 8 * c8);
+            for (int k = 0; k < 4; ++k) split2(S[8 * c8 + 2 * k], S[8 * c8 + 2 * k + 1], whi[k], wlo[k]);
+            const uint32_t off = sw128(i, kCW * cg + 8 * c8);
             *reinterpret_cast<uint4*>(sm + Smem::SHI + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
             *reinterpret_cast<uint4*>(sm + Smem::SLO + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
         }
     };
-    if (q < 2) store_state();
+    if (!producer && q < 2) store_state();
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -252,308 +279,331 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const uint32_t tmem = *slot;
     const uint32_t tG = tmem, tYi = tmem + 128, tYe = tmem + 192, tDS = tmem + 256;
 
-    auto issue_a = [&](int c) {
-        const int t0 = c * kQ;
-        mbar_arrive_expect_tx(bar_a, Smem::TX_A);
-        tma_load_3d(sm + Smem::XR, &tm_x, bar_a, h * kP, t0 - 3, b);
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-                tma_load_3d(sm + (k ? Smem::BTLO : Smem::BTHI) + r * 8192, &tm_bt, bar_a, t0 + 64 * r, 0,
-                            k * BG + bg);
-    };
-    auto issue_b_tiles = [&](int c) {
-        const int t0 = c * kQ;
-        mbar_arrive_expect_tx(bar_b, Smem::TX_B);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tma_load_3d(sm + 16384 * k, &tm_bc, bar_b, 0, t0, k * BG + bg);
-    };
-    auto issue_b_z = [&](int c) { tma_load_3d(sm + Smem::ZT, &tm_z, bar_b, h * kP, c * kQ, b); };
-    if (tid == 0) {
-        issue_a(0);
-        issue_b_tiles(0);
-        issue_b_z(0);
-    }
-
-    int waited_a = 0, waited_b = 0, issued_a = 1, issued_b = 1, mma_wait = 0;
-    bool bad = false;
-    float xv[32];                                    // x of (token i, positions 32 hf ..), fp32
-    for (int c = 0; c < nch && !bad; ++c) {
-        const int t0 = c * kQ;
-        // ---- raw x and B^T of the chunk
-        bool ok = mbar_wait_bounded(bar_a, (uint32_t)(waited_a & 1));
-        ++waited_a;
-        if (__syncthreads_or(!ok)) { bad = true; break; }
-
-        // ---- delta and the chunk-local cumulative decay exponent s (in log2 units)
-        if (hf == 0) {
-            const int t = t0 + i;
-            float dl = 0.f;
-            if (t < L) dl = softplus_in<Tin_bf16>(to_f32(dtp[(int64_t)t * p.dt_stride_t]) + bias);
-            float v = dl * A2;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
-            }
-            if (lane == 31) s_ws[q] = v;
-            s_dl[i] = dl;
-            s_cs[i] = v;
-        }
-        __syncthreads();
-        if (hf == 0) {
-            float off = 0.f;
-            for (int k = 0; k < q; ++k) off += s_ws[k];
-            s_cs[i] += off;
-        }
-        __syncthreads();
-        const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
-
-        // ---- conv + SiLU of x (token i, positions 32 hf ..), written as X^T hi/lo and the
-        //      state-update operand w_i x_i (w_i = 2^(s_Q - s_i) delta_i), hi rows / lo rows
-        {
-            float r[4][32];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int row = i + k;                    // tile row of token t0 + i - 3 + k
-                if (c == 0 && row < 3 && p.conv_state_in) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        r[k][e] = p.conv_state_in[((int64_t)b * 3 + row) * Cx + h * (int64_t)kP + 32 * hf + e];
-                } else {
-                    const uint4* src = reinterpret_cast<const uint4*>(sm + Smem::XR + row * 128 + 64 * hf);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint4 u = src[e];
-                        const uint32_t ws4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int f = 0; f < 4; ++f) {
-                            r[k][8 * e + 2 * f] = __uint_as_float(ws4[f] << 16);
-                            r[k][8 * e + 2 * f + 1] = __uint_as_float(ws4[f] & 0xffff0000u);
-                        }
-                    }
+    if (producer) {
+        if (lane == 0) {
+            auto issue_a = [&](int c) {              // raw x (with the 3-token halo) and B^T hi/lo
+                const int t0 = c * kQ;
+                mbar_arrive_expect_tx(&bars[kBarA], Smem::TX_A);
+                tma_load_3d(sm + Smem::XR, &tm_x, &bars[kBarA], h * kP, t0 - 3, b);
+                for (int k = 0; k < 2; ++k)
+                    for (int r = 0; r < 2; ++r)
+                        tma_load_3d(sm + (k ? Smem::BTLO : Smem::BTHI) + r * 8192, &tm_bt, &bars[kBarA],
+                                    t0 + 64 * r, 0, k * BG + bg);
+            };
+            auto issue_b = [&](int c) {              // C hi, C lo, B hi, B lo
+                mbar_arrive_expect_tx(&bars[kBarB], 4 * 16384);
+                for (int k = 0; k < 4; ++k) tma_load_3d(sm + 16384 * k, &tm_bc, &bars[kBarB], 0, c * kQ, k * BG + bg);
+            };
+            auto issue_z = [&](int c) {
+                mbar_arrive_expect_tx(&bars[kBarZ], kQ * kP * 2);
+                tma_load_3d(sm + Smem::ZT, &tm_z, &bars[kBarZ], h * kP, c * kQ, b);
+            };
+            // phase parity of the c-th completion of a once-per-chunk barrier
+            auto wait = [&](int k, int c) -> bool {
+                if (mbar_wait_bounded(&bars[k], (uint32_t)(c & 1))) return true;
+                *reinterpret_cast<volatile int*>(s_err) = 1;
+                atomicOr(p.status, 1u);
+                return false;
+            };
+            int ia = 1, ib = 1, iz = 1;              // copies issued per group
+            int ng = 0, nd = 0, ny = 0;              // MMA groups committed
+            issue_b(0);
+            issue_a(0);
+            issue_z(0);
+            int c = 0;
+            for (; c < nch; ++c) {
+                if (!wait(kBarB, c)) break;
+                if (c > 0) {
+                    if (!wait(kDone, c - 1)) break;  // every worker is past chunk c-1
+                    issue_z(c);
+                    ++iz;
                 }
-            }
-            const float wi = ex2(s_Q - s_i) * dl_i;
-            const int reg = i >> 6, col = i & 63;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int pp = 32 * hf + e;
-                const float* w = s_cw + 4 * pp;
-                float xc = fmaf(w[0], r[0][e], s_cb[pp]);
-                xc = fmaf(w[1], r[1][e], xc);
-                xc = fmaf(w[2], r[2][e], xc);
-                xc = fmaf(w[3], r[3][e], xc);
-                const float u = silu_in<Tin_bf16>(xc);
-                xv[e] = u;
-                __nv_bfloat16 hi, lo;
-                split_bf16(u, hi, lo);
-                st_u16(sm, Smem::XHI + reg * 8192 + sw128(pp, col), hi);
-                st_u16(sm, Smem::XLO + reg * 8192 + sw128(pp, col), lo);
-                split_bf16(wi * u, hi, lo);
-                st_u16(sm, Smem::XW + reg * 16384 + sw128(pp, col), hi);
-                st_u16(sm, Smem::XW + reg * 16384 + sw128(64 + pp, col), lo);
-            }
-        }
-        fence_proxy_async_smem();
-
-        // ---- C, B tiles and z of the chunk
-        ok = mbar_wait_bounded(bar_b, (uint32_t)(waited_b & 1));
-        ++waited_b;
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) { bad = true; break; }
-        if (tid == 0) {
-            tc_fence_after();
-            // G = C B^T
-            mma_k64(tG, sb + Smem::CHI, sb + Smem::BHI, kIdescN128, true);
-            mma_k64(tG, sb + Smem::CHI, sb + Smem::BLO, kIdescN128, false);
-            mma_k64(tG, sb + Smem::CLO, sb + Smem::BHI, kIdescN128, false);
-            // Y_inter = C S_prev^T
-            mma_k64(tYe, sb + Smem::CHI, sb + Smem::SHI, kIdescN64, true);
-            mma_k64(tYe, sb + Smem::CHI, sb + Smem::SLO, kIdescN64, false);
-            mma_k64(tYe, sb + Smem::CLO, sb + Smem::SHI, kIdescN64, false);
-            // dS^T = (w x)^T B over the chunk's 128 tokens: rows 0-63 from the hi part of w x,
-            // rows 64-127 from its lo part, each times B hi + B lo
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-#pragma unroll
+                tc_fence_after();
+                mma_k64(tG, sb + Smem::CHI, sb + Smem::BHI, kIdescN128, true);
+                mma_k64(tG, sb + Smem::CHI, sb + Smem::BLO, kIdescN128, false);
+                mma_k64(tG, sb + Smem::CLO, sb + Smem::BHI, kIdescN128, false);
+                mma_k64(tYe, sb + Smem::CHI, sb + Smem::SHI, kIdescN64, true);
+                mma_k64(tYe, sb + Smem::CHI, sb + Smem::SLO, kIdescN64, false);
+                mma_k64(tYe, sb + Smem::CLO, sb + Smem::SHI, kIdescN64, false);
+                mma_commit(&bars[kBarG]);
+                ++ng;
+                if (!wait(kXReady, c)) break;
+                tc_fence_after();
+                // dS^T = (w x)^T B: rows 0-63 from the hi part of w x, rows 64-127 from its lo part
+                for (int k = 0; k < 2; ++k)
+                    for (int r = 0; r < 2; ++r)
+                        mma_k64(tDS, sb + Smem::XW + r * 16384, sb + (k ? Smem::BTLO : Smem::BTHI) + r * 8192,
+                                kIdescN64, k == 0 && r == 0);
+                mma_commit(&bars[kBarD]);
+                ++nd;
+                if (!wait(kMReady, c)) break;
+                tc_fence_after();
                 for (int r = 0; r < 2; ++r)
-                    mma_k64(tDS, sb + Smem::XW + r * 16384, sb + (k ? Smem::BTLO : Smem::BTHI) + r * 8192, kIdescN64,
-                            k == 0 && r == 0);
-            mma_commit(bar_m);
-        }
-        ok = mbar_wait_bounded(bar_m, (uint32_t)(mma_wait & 1));
-        ++mma_wait;
-        if (__syncthreads_or(!ok)) { bad = true; break; }
-        tc_fence_after();
-        if (tid == 0 && c + 1 < nch) {               // raw x and B^T of the chunk are consumed
-            issue_a(c + 1);
-            ++issued_a;
-        }
-
-        // ---- M = G exp(s_i - s_j) delta_j (j <= i) as hi/lo, over the C and B tiles
-        {
-            const int j0 = 64 * hf;
-            const uint32_t mh = Smem::MHI + hf * 16384, ml = Smem::MLO + hf * 16384;
-            if (j0 > 32 * q + 31) {
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint32_t off = (uint32_t)(i * 128 + ((c8 ^ (i & 7)) << 4));
-                    *reinterpret_cast<uint4*>(sm + mh + off) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(sm + ml + off) = make_uint4(0, 0, 0, 0);
-                }
-            } else {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[32];
-                    tmem_ld32(tG + ((uint32_t)(32 * q) << 16) + (uint32_t)(j0 + 32 * half), v);
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        uint32_t whi[4], wlo[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            __nv_bfloat16 hh[2], ll[2];
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int jl = 8 * c8 + 2 * k + e, j = j0 + 32 * half + jl;
-                                const float m = j <= i ? v[jl] * ex2(s_i - s_cs[j]) * s_dl[j] : 0.f;
-                                split_bf16(m, hh[e], ll[e]);
-                            }
-                            whi[k] = pack2(hh[0], hh[1]);
-                            wlo[k] = pack2(ll[0], ll[1]);
-                        }
-                        const int ch = 4 * half + c8;
-                        const uint32_t off = (uint32_t)(i * 128 + ((ch ^ (i & 7)) << 4));
-                        *reinterpret_cast<uint4*>(sm + mh + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-                        *reinterpret_cast<uint4*>(sm + ml + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
-                    }
+                    mma_k64(tYi, sb + Smem::MHI + r * 16384, sb + Smem::XHI + r * 8192, kIdescN64, r == 0);
+                for (int r = 0; r < 2; ++r)
+                    mma_k64(tYi, sb + Smem::MHI + r * 16384, sb + Smem::XLO + r * 8192, kIdescN64, false);
+                for (int r = 0; r < 2; ++r)
+                    mma_k64(tYi, sb + Smem::MLO + r * 16384, sb + Smem::XHI + r * 8192, kIdescN64, false);
+                mma_commit(&bars[kBarY]);
+                ++ny;
+                if (c + 1 < nch) {
+                    if (!wait(kBarD, c)) break;      // raw x (conv done) and B^T (dS done) are free
+                    issue_a(c + 1);
+                    ++ia;
+                    if (!wait(kBarY, c)) break;      // M over C, B (and G, Y_inter) are consumed
+                    issue_b(c + 1);
+                    ++ib;
                 }
             }
-        }
-
-        // ---- state: S = 2^(s_Q) S + dS (hi part rows + lo part rows of the accumulator)
-        {
-            float v[32];
-            tmem_ld32(tDS + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * hf), v);
-            float* scr = reinterpret_cast<float*>(sm + Smem::XW);
-            if (q >= 2) {
-                float4* dst = reinterpret_cast<float4*>(scr + (i - 64) * Smem::SCR_LD + 32 * hf);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            if (c < nch) {
+                // stopped early: let every copy and MMA group still in flight finish (its last
+                // completion) before shared memory and TMEM go away
+                const int last[6] = {ia, ib, iz, ng, nd, ny};
+                for (int k = 0; k < 6; ++k)
+                    if (last[k] > 0) (void)mbar_wait_bounded(&bars[k], (uint32_t)((last[k] - 1) & 1), 100000000ull);
             }
-            tc_fence_before();
-            __syncthreads();
-            if (q < 2) {
-                const float eQ = ex2(s_Q);
-                const float4* src = reinterpret_cast<const float4*>(scr + i * Smem::SCR_LD + 32 * hf);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float4 o = src[k];
-                    S[4 * k] = fmaf(eQ, S[4 * k], v[4 * k] + o.x);
-                    S[4 * k + 1] = fmaf(eQ, S[4 * k + 1], v[4 * k + 1] + o.y);
-                    S[4 * k + 2] = fmaf(eQ, S[4 * k + 2], v[4 * k + 2] + o.z);
-                    S[4 * k + 3] = fmaf(eQ, S[4 * k + 3], v[4 * k + 3] + o.w);
-                }
-                store_state();
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- Y_intra = M X
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-                mma_k64(tYi, sb + Smem::MHI + r * 16384, sb + Smem::XHI + r * 8192, kIdescN64, r == 0);
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-                mma_k64(tYi, sb + Smem::MHI + r * 16384, sb + Smem::XLO + r * 8192, kIdescN64, false);
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-                mma_k64(tYi, sb + Smem::MLO + r * 16384, sb + Smem::XHI + r * 8192, kIdescN64, false);
-            mma_commit(bar_m);
-        }
-        ok = mbar_wait_bounded(bar_m, (uint32_t)(mma_wait & 1));
-        ++mma_wait;
-        if (__syncthreads_or(!ok)) { bad = true; break; }
-        tc_fence_after();
-        if (tid == 0 && c + 1 < nch) issue_b_tiles(c + 1);   // M (over C and B) is consumed
-
-        // ---- out = (Y_intra + 2^(s_i) Y_inter + D x) SiLU(z)
-        {
-            float yi[32], ye[32];
-            tmem_ld32(tYi + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * hf), yi);
-            tmem_ld32(tYe + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * hf), ye);
-            const float ei = ex2(s_i);
-            const int t = t0 + i;
-            float o[32];
-            const uint4* zs = reinterpret_cast<const uint4*>(sm + Smem::ZT + i * 128 + 64 * hf);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint4 u = zs[e];
-                const uint32_t ws4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const int k = 8 * e + 2 * f;
-                    const float z0 = __uint_as_float(ws4[f] << 16), z1 = __uint_as_float(ws4[f] & 0xffff0000u);
-                    o[k] = fmaf(ei, ye[k], yi[k] + Dh * xv[k]) * silu_in<Tin_bf16>(z0);
-                    o[k + 1] = fmaf(ei, ye[k + 1], yi[k + 1] + Dh * xv[k + 1]) * silu_in<Tin_bf16>(z1);
-                }
-            }
-            if (t < L) {
-                Tout* dst = reinterpret_cast<Tout*>(p.out) + (int64_t)b * p.out_stride_b + (int64_t)t * p.out_stride_t +
-                            (int64_t)h * kP + 32 * hf;
-                if constexpr (sizeof(Tout) == 4) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        reinterpret_cast<float4*>(dst)[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int f = 0; f < 4; ++f)
-                            w4[f] = pack2(__float2bfloat16_rn(o[8 * k + 2 * f]), __float2bfloat16_rn(o[8 * k + 2 * f + 1]));
-                        reinterpret_cast<uint4*>(dst)[k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    }
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && c + 1 < nch) {               // z of the chunk is consumed
-            issue_b_z(c + 1);
-            ++issued_b;
-        }
-    }
-
-    if (bad) {
-        if (tid == 0) {
-            atomicOr(p.status, 1u);
-            // let every copy still in flight land before the CTA's shared memory goes away
-            if (issued_a > waited_a) (void)mbar_wait_bounded(bar_a, (uint32_t)(waited_a & 1), 100000000ull);
-            if (issued_b > waited_b) (void)mbar_wait_bounded(bar_b, (uint32_t)(waited_b & 1), 100000000ull);
-            (void)mbar_wait_bounded(bar_m, (uint32_t)(mma_wait & 1), 100000000ull);
         }
     } else {
-        // final SSM state and the x channels' conv window
-        if (q < 2) {
-            float4* dst = reinterpret_cast<float4*>(p.ssm_state_out + (((int64_t)b * H + h) * kP + i) * kNs + 32 * hf);
+        float* s_dl2 = reinterpret_cast<float*>(sm + Smem::DL);   // [2][128]: delta by chunk parity
+        float* s_cs2 = reinterpret_cast<float*>(sm + Smem::CS);   // [2][128]: s by chunk parity
+        bool bad = false;
+        auto wait = [&](int k, int c) {
+            if (!bad && !mbar_wait_bounded(&bars[k], (uint32_t)(c & 1))) {
+                bad = true;
+                atomicOr(p.status, 1u);
+            }
+        };
+        auto arrive = [&](int k) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[k]);
+        };
+        float dt_next = (cg == 0 && i < L) ? to_f32(dtp[(int64_t)i * p.dt_stride_t]) : 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const int t0 = c * kQ;
+            float* s_dl = s_dl2 + (c & 1) * kQ;
+            float* s_cs = s_cs2 + (c & 1) * kQ;
+            const float dt_i = dt_next;
+            if (cg == 0 && c + 1 < nch && t0 + kQ + i < L) dt_next = to_f32(dtp[(int64_t)(t0 + kQ + i) * p.dt_stride_t]);
+
+            // ---- 2. delta, s (chunk-local cumulative delta A, log2 units), conv + SiLU of x
+            wait(kBarA, c);
+            if (cg == 0) {
+                const int t = t0 + i;
+                float dl = 0.f;
+                if (t < L) dl = softplus_in<Tin_bf16>(dt_i + bias);
+                float v = dl * A2;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) dst[k] = make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += u;
+                }
+                if (lane == 31) s_ws[q] = v;
+                s_dl[i] = dl;
+                s_cs[i] = v;
+            }
+            if (workers_any(bad)) {
+                bad = true;
+                break;
+            }
+            if (cg == 0) {
+                float off = 0.f;
+                for (int k = 0; k < q; ++k) off += s_ws[k];
+                s_cs[i] += off;
+            }
+            workers_sync();
+            const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
+            {
+                // x of token i, positions kCW cg .., written as X^T hi/lo and as the state-update
+                // operand w_i x_i (w_i = 2^(s_Q - s_i) delta_i): hi rows 0-63, lo rows 64-127
+                float r[4][kCW];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = i + k;                    // tile row of token t0 + i - 3 + k
+                    if (c == 0 && row < 3 && p.conv_state_in) {
+#pragma unroll
+                        for (int e = 0; e < kCW; ++e)
+                            r[k][e] = p.conv_state_in[((int64_t)b * 3 + row) * Cx + h * (int64_t)kP + kCW * cg + e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < kCW / 8; ++e) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(
+                                sm + Smem::XR + row * 128 + (((((kCW / 8) * cg + e) ^ (row & 7))) << 4));
+                            const uint32_t ws4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int f = 0; f < 4; ++f) {
+                                r[k][8 * e + 2 * f] = __uint_as_float(ws4[f] << 16);
+                                r[k][8 * e + 2 * f + 1] = __uint_as_float(ws4[f] & 0xffff0000u);
+                            }
+                        }
+                    }
+                }
+                const float wi = ex2(s_Q - s_i) * dl_i;
+                const int reg = i >> 6, col = i & 63;
+#pragma unroll
+                for (int e = 0; e < kCW; ++e) {
+                    const int pp = kCW * cg + e;
+                    const float* w = s_cw + 4 * pp;
+                    float xc = fmaf(w[0], r[0][e], s_cb[pp]);
+                    xc = fmaf(w[1], r[1][e], xc);
+                    xc = fmaf(w[2], r[2][e], xc);
+                    xc = fmaf(w[3], r[3][e], xc);
+                    const float u = silu_in<Tin_bf16>(xc);
+                    uint32_t hi, lo;
+                    split2(u, wi * u, hi, lo);           // (x, w x) hi pair and lo pair
+                    const uint32_t o1 = sw128(pp, col);
+                    *reinterpret_cast<uint16_t*>(sm + Smem::XHI + reg * 8192 + o1) = (uint16_t)hi;
+                    *reinterpret_cast<uint16_t*>(sm + Smem::XLO + reg * 8192 + o1) = (uint16_t)lo;
+                    *reinterpret_cast<uint16_t*>(sm + Smem::XW + reg * 16384 + o1) = (uint16_t)(hi >> 16);
+                    *reinterpret_cast<uint16_t*>(sm + Smem::XW + reg * 16384 + sw128(64 + pp, col)) = (uint16_t)(lo >> 16);
+                }
+            }
+            fence_proxy_async_smem();
+            arrive(kXReady);
+
+            // ---- 3. M = G 2^(s_i - s_j) delta_j (j < i), M[i][i] = G[i][i] delta_i + D, as hi/lo
+            //      over the C and B tiles: columns [kMJ cg, kMJ cg + kMJ) of row i
+            wait(kBarG, c);
+            tc_fence_after();
+            {
+                const int j0 = kMJ * cg;
+                if (j0 > 32 * q + 31) {                  // entirely above the diagonal
+#pragma unroll
+                    for (int c8 = 0; c8 < kMJ / 8; ++c8) {
+                        const int jj = j0 + 8 * c8;
+                        const uint32_t off = (uint32_t)((jj >> 6) * 16384 + i * 128 + ((((jj & 63) >> 3) ^ (i & 7)) << 4));
+                        *reinterpret_cast<uint4*>(sm + Smem::MHI + off) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(sm + Smem::MLO + off) = make_uint4(0, 0, 0, 0);
+                    }
+                } else {
+#pragma unroll
+                    for (int half = 0; half < kMJ / 32; ++half) {
+                        const int jb = j0 + 32 * half;
+                        float v[32];
+                        tmem_ld32(tG + ((uint32_t)(32 * q) << 16) + (uint32_t)jb, v);
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const float4 sa = *reinterpret_cast<const float4*>(s_cs + jb + 8 * c8);
+                            const float4 sb4 = *reinterpret_cast<const float4*>(s_cs + jb + 8 * c8 + 4);
+                            const float4 da = *reinterpret_cast<const float4*>(s_dl + jb + 8 * c8);
+                            const float4 db4 = *reinterpret_cast<const float4*>(s_dl + jb + 8 * c8 + 4);
+                            const float sj[8] = {sa.x, sa.y, sa.z, sa.w, sb4.x, sb4.y, sb4.z, sb4.w};
+                            const float dj[8] = {da.x, da.y, da.z, da.w, db4.x, db4.y, db4.z, db4.w};
+                            float m[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int jl = 8 * c8 + e, j = jb + jl;
+                                // the skip term D x_i rides on the diagonal: Y = M X then includes it
+                                m[e] = j < i ? v[jl] * ex2(s_i - sj[e]) * dj[e] : (j == i ? fmaf(v[jl], dl_i, Dh) : 0.f);
+                            }
+                            uint32_t whi[4], wlo[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) split2(m[2 * k], m[2 * k + 1], whi[k], wlo[k]);
+                            const int jj = jb + 8 * c8;
+                            const uint32_t off = (uint32_t)((jj >> 6) * 16384 + i * 128 + ((((jj & 63) >> 3) ^ (i & 7)) << 4));
+                            *reinterpret_cast<uint4*>(sm + Smem::MHI + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+                            *reinterpret_cast<uint4*>(sm + Smem::MLO + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            arrive(kMReady);
+
+            // ---- 4. state: S = 2^(s_Q) S + dS (the accumulator's hi-part rows + lo-part rows)
+            wait(kBarD, c);
+            tc_fence_after();
+            {
+                float v[kCW];
+                tmem_ld16(tDS + ((uint32_t)(32 * q) << 16) + (uint32_t)(kCW * cg), v);
+                float* scr = reinterpret_cast<float*>(sm + Smem::XW);   // w x is consumed by dS
+                if (q >= 2) {
+                    float4* dst = reinterpret_cast<float4*>(scr + (i - 64) * Smem::SCR_LD + kCW * cg);
+#pragma unroll
+                    for (int k = 0; k < kCW / 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                }
+                tc_fence_before();
+                workers_sync();
+                if (q < 2) {
+                    const float eQ = ex2(s_Q);
+                    const float4* src = reinterpret_cast<const float4*>(scr + i * Smem::SCR_LD + kCW * cg);
+#pragma unroll
+                    for (int k = 0; k < kCW / 4; ++k) {
+                        const float4 o = src[k];
+                        S[4 * k] = fmaf(eQ, S[4 * k], v[4 * k] + o.x);
+                        S[4 * k + 1] = fmaf(eQ, S[4 * k + 1], v[4 * k + 1] + o.y);
+                        S[4 * k + 2] = fmaf(eQ, S[4 * k + 2], v[4 * k + 2] + o.z);
+                        S[4 * k + 3] = fmaf(eQ, S[4 * k + 3], v[4 * k + 3] + o.w);
+                    }
+                    store_state();                       // Y_inter, its reader, completed with G
+                }
+            }
+            fence_proxy_async_smem();
+
+            // ---- 5. out = (Y_intra + 2^(s_i) Y_inter) SiLU(z)   (Y_intra holds D x through M's diagonal)
+            wait(kBarY, c);
+            wait(kBarZ, c);
+            tc_fence_after();
+            {
+                float yi[kCW], ye[kCW];
+                tmem_ld16(tYi + ((uint32_t)(32 * q) << 16) + (uint32_t)(kCW * cg), yi);
+                tmem_ld16(tYe + ((uint32_t)(32 * q) << 16) + (uint32_t)(kCW * cg), ye);
+                const float ei = ex2(s_i);
+                const int t = t0 + i;
+                float o[kCW];
+#pragma unroll
+                for (int e = 0; e < kCW / 8; ++e) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(sm + Smem::ZT + i * 128 + ((((kCW / 8) * cg + e) ^ (i & 7)) << 4));
+                    const uint32_t ws4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const int k = 8 * e + 2 * f;
+                        const float z0 = __uint_as_float(ws4[f] << 16), z1 = __uint_as_float(ws4[f] & 0xffff0000u);
+                        o[k] = fmaf(ei, ye[k], yi[k]) * silu_in<Tin_bf16>(z0);
+                        o[k + 1] = fmaf(ei, ye[k + 1], yi[k + 1]) * silu_in<Tin_bf16>(z1);
+                    }
+                }
+                if (t < L && !bad) {
+                    Tout* dst = reinterpret_cast<Tout*>(p.out) + (int64_t)b * p.out_stride_b + (int64_t)t * p.out_stride_t +
+                                (int64_t)h * kP + kCW * cg;
+                    if constexpr (sizeof(Tout) == 4) {
+#pragma unroll
+                        for (int k = 0; k < kCW / 4; ++k)
+                            reinterpret_cast<float4*>(dst)[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kCW / 8; ++k) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int f = 0; f < 4; ++f)
+                                w4[f] = pack2(__float2bfloat16_rn(o[8 * k + 2 * f]), __float2bfloat16_rn(o[8 * k + 2 * f + 1]));
+                            reinterpret_cast<uint4*>(dst)[k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            arrive(kDone);
         }
-        if (tid < 3 * kP) {
-            const int k = tid / kP, pp = tid % kP, t = L - 3 + k;
-            const int64_t ch = h * (int64_t)kP + pp;
-            float v = 0.f;
-            if (t >= 0)
-                v = to_f32(reinterpret_cast<const Tin_bf16*>(p.xBC)[(int64_t)b * p.xbc_stride_b + (int64_t)t * p.xbc_stride_t + ch]);
-            else if (p.conv_state_in)
-                v = p.conv_state_in[((int64_t)b * 3 + 3 + t) * Cx + ch];
-            p.conv_state_out[((int64_t)b * 3 + k) * Cx + ch] = v;
+        if (bad) {
+            if (tid == 0) atomicOr(p.status, 1u);
+        } else {
+            // final SSM state and the x channels' conv window
+            if (q < 2) {
+                float4* dst = reinterpret_cast<float4*>(p.ssm_state_out + (((int64_t)b * H + h) * kP + i) * kNs + kCW * cg);
+#pragma unroll
+                for (int k = 0; k < kCW / 4; ++k) dst[k] = make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]);
+            }
+            if (tid < 3 * kP) {
+                const int k = tid / kP, pp = tid % kP, t = L - 3 + k;
+                const int64_t ch = h * (int64_t)kP + pp;
+                float v = 0.f;
+                if (t >= 0)
+                    v = to_f32(reinterpret_cast<const Tin_bf16*>(p.xBC)[(int64_t)b * p.xbc_stride_b + (int64_t)t * p.xbc_stride_t + ch]);
+                else if (p.conv_state_in)
+                    v = p.conv_state_in[((int64_t)b * 3 + 3 + t) * Cx + ch];
+                p.conv_state_out[((int64_t)b * 3 + k) * Cx + ch] = v;
+            }
         }
     }
     tc_fence_before();
@@ -693,10 +743,12 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
     const uint64_t xs_b = a.batch > 1 ? (uint64_t)a.xbc_stride_b * 2 : (uint64_t)L * a.xbc_stride_t * 2;
     const uint64_t zs_b = a.batch > 1 ? (uint64_t)a.z_stride_b * 2 : (uint64_t)L * a.z_stride_t * 2;
     const unsigned char* ws = static_cast<const unsigned char*>(a.workspace);
+    // raw x and z arrive 128-byte swizzled, so that a lane reading its own token row of 128 bytes
+    // hits all 32 banks across a warp
     if (!make_map3(&mx, a.xBC, (uint64_t)Cx, (uint64_t)L, (uint64_t)a.batch, (uint64_t)a.xbc_stride_t * 2, xs_b, kP,
-                   kQ + 3, false) ||
+                   kQ + 3, true) ||
         !make_map3(&mz, a.z, (uint64_t)HP, (uint64_t)L, (uint64_t)a.batch, (uint64_t)a.z_stride_t * 2, zs_b, kP, kQ,
-                   false) ||
+                   true) ||
         !make_map3(&mbc, ws, kNs, (uint64_t)L, (uint64_t)(4 * BG), kNs * 2, (uint64_t)L * kNs * 2, kNs, kQ, true) ||
         !make_map3(&mbt, ws + w.bt_off, (uint64_t)L, kNs, (uint64_t)(2 * BG), (uint64_t)w.lp * 2,
                    (uint64_t)w.lp * kNs * 2, 64, kNs, true)) {
@@ -718,7 +770,7 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
         }
         __atomic_fetch_or(&done[out_bf16], bit, __ATOMIC_ACQ_REL);
     }
-    kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kTh, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, a);
+    kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kThAll, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
