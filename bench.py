@@ -340,6 +340,7 @@ def run_ours(args):
         extras["decode_block"] = bench_decode_block(ssm, dev, stream, hbm_peak, flush)
         extras["out_proj"] = bench_out_proj(ssm, dev, stream, flush, _tc_peak())
         extras["decode_configs"] = bench_decode_configs(ssm, dev, stream, hbm_peak)
+        extras["ssd"] = bench_ssd(ssm, dev, stream, hbm_peak, flush, _tc_peak())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -547,6 +548,107 @@ def bench_out_proj(ssm, dev, stream, flush, tc_peak):
         torch.cuda.empty_cache()
     res["note"] = ("k_out_proj: tcgen05.mma kind::f16, 128x256 tiles, 4-stage TMA ring, TMEM accumulator; "
                    "frac_tensor against MEASURED_PEAKS.json bf16_tflops (burst); cuBLAS is context, not used")
+    return res
+
+
+def ssd_prefill_bytes(B, L, H, G, P=64, N=64, out_es=4):
+    """Algorithmic bytes of one SSD prefill: bf16 xBC, z, dt read once, out written once, fp32
+    params read once, final conv and SSM states written once."""
+    Cx = H * P + 2 * G * N
+    per_token = Cx * 2 + H * P * 2 + H * 2 + H * P * out_es
+    params = Cx * 4 * 5 + H * 4 * 3
+    states = B * (3 * Cx * 4 + H * P * N * 4)
+    return B * L * per_token + params + states
+
+
+def ssd_prefill_mma_flops(B, L, H, P=64, N=64, Q=128):
+    """Tensor-core work of the chunked SSD form as the kernel runs it, per 128-token chunk and head:
+    G = C B^T (128 x 128 x N) and Y_intra = M X (128 x 64 x 128), Y_inter = C S^T (128 x 64 x N),
+    each three hi/lo products, and the state update (128 x N x 128) as four."""
+    chunks = B * H * ((L + Q - 1) // Q)
+    per_chunk = 2 * (3 * Q * Q * N + 3 * Q * P * Q + 3 * Q * P * N + 2 * 2 * P * N * Q)
+    return chunks * per_chunk
+
+
+def bench_ssd(ssm, dev, stream, hbm_peak, flush, tc_peak):
+    """The SSD (Mamba-2-style) mixer: ssd_prefill on the Zamba2-2.7B-like layer (4 x 2048 tokens,
+    80 heads of 64, d_state 64, one group) and on a Zamba2-7B-like batch-1 prompt (16384 tokens,
+    112 heads), L2 flushed before each of 10 timed launches; ssd_decode_step at batch 64 and 256
+    of the 80-head layer (CUDA graph of back-to-back steps, state [64 x 64] per request and head)."""
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_ssd_inputs, make_ssd_states
+    res = {}
+    for name, (B, L, H, G) in {"zamba2_2p7b_like_layer_b4_l2048_h80": (4, 2048, 80, 1),
+                               "zamba2_7b_like_prompt_b1_l16384_h112": (1, 16384, 112, 1)}.items():
+        inp = make_ssd_inputs(B, L, H, n_groups=G, seed=0, device=dev)
+        out = torch.empty(B, L, 64 * H, device=dev)
+        cso = torch.empty(B, 3, inp.channels, device=dev)
+        sso = torch.empty(B, H, 64, 64, device=dev)
+        ws = torch.empty(ssm.ssd_prefill_workspace_bytes(B, L, G), device=dev, dtype=torch.uint8)
+        f = lambda: ssm.ssd_prefill(inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H,
+                                    G, out=out, conv_state_out=cso, ssm_state_out=sso, workspace=ws, stream=stream)
+        for _ in range(3):
+            f()
+        ts = []
+        for k in range(10):
+            flush.fill_(float(k))
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            f()
+            b_.record(stream)
+            ts.append((a, b_))
+        torch.cuda.synchronize(dev)
+        t = statistics.median(a.elapsed_time(b_) for a, b_ in ts) / 1e3
+        byts = ssd_prefill_bytes(B, L, H, G)
+        fl = ssd_prefill_mma_flops(B, L, H)
+        res[name] = {"us": 1e6 * t, "tokens_per_s": B * L / t, "GB_s": byts / t / 1e9,
+                     "frac_hbm": byts / t / 1e9 / hbm_peak, "mma_TFLOP_s": fl / t / 1e12,
+                     "frac_tensor": fl / t / 1e12 / tc_peak}
+        del inp, out, cso, sso, ws
+        torch.cuda.empty_cache()
+    H, G = 80, 1
+    for batch in (64, 256):
+        inp = make_ssd_inputs(batch, 1, H, n_groups=G, seed=batch, device=dev)
+        cs, ss = (t.to(dev) for t in make_ssd_states(batch, H, 64, 64, inp.channels, seed=batch))
+        xb, z, dt = inp.xBC[:, 0].contiguous(), inp.z[:, 0].contiguous(), inp.dt[:, 0].contiguous()
+        out = torch.empty(batch, 64 * H, device=dev)
+        steps = 32
+
+        def one():
+            ssm.ssd_decode_step(xb, z, dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G, cs, ss, out=out,
+                                stream=torch.cuda.current_stream(dev))
+
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                one()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(steps):
+                one()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        t = a.elapsed_time(b_) / 1e3 / (reps * steps)
+        Cx = inp.channels
+        byts = batch * (H * 64 * 64 * 4 * 2 + 3 * Cx * 4 * 2 + Cx * 2 + 64 * H * 2 + H * 2 + 64 * H * 4)
+        res[f"decode_b{batch}_h80"] = {"us_per_step": 1e6 * t, "steps_per_s": 1 / t, "GB_s": byts / t / 1e9,
+                                       "frac_hbm": byts / t / 1e9 / hbm_peak}
+        del g
+    res["note"] = ("k_ssd_bc (B, C conv + hi/lo planes) + k_ssd_chunk (tcgen05: G = C B^T, M X, C S^T and the "
+                   "state update on bf16 hi/lo operand pairs, fp32 TMEM accumulators; a producer warp issues "
+                   "TMA and MMA, 16 worker warps the arithmetic).  frac_hbm is against algorithmic bytes; "
+                   "mma_TFLOP_s counts the hi/lo products the kernel issues (frac_tensor of the measured bf16 "
+                   "peak); decode: k_ssd_decode + k_ssd_decode_shift per step, L2-resident state at batch 64")
     return res
 
 

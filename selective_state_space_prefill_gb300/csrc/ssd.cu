@@ -59,6 +59,10 @@ static_assert(kCW % 8 == 0 && kMJ % 32 == 0, "column split");
 // M = 128, N = 128 or 64.
 constexpr uint32_t kIdescN128 = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) | (8u << 24);
 constexpr uint32_t kIdescN64 = (1u << 4) | (1u << 7) | (1u << 10) | (8u << 17) | (8u << 24);
+// ... with A (bit 15) or B (bit 16) MN-major: the operand's rows run along K, its M or N
+// elements contiguous in each 128-byte row
+constexpr uint32_t kIdescN64_AMN = kIdescN64 | (1u << 15);
+constexpr uint32_t kIdescN64_BMN = kIdescN64 | (1u << 16);
 
 // Shared memory of k_ssd_chunk (byte offsets from a 1024-aligned base).  Operand tiles are
 // K-major rows of 64 bf16 (128 bytes) in 128-byte-swizzle atoms; a K extent of 128 is two such
@@ -67,9 +71,9 @@ struct Smem {
     static constexpr int CHI = 0, CLO = 16384, BHI = 32768, BLO = 49152;  // [128 t][64 n] (TMA)
     static constexpr int MHI = 0, MLO = 32768;       // M hi / lo, r0 and r1 [128 i][64 j] each (over C, B)
     static constexpr int BTHI = 65536, BTLO = 81920; // B^T hi / lo, r0 and r1 [64 n][64 t] each (TMA)
-    static constexpr int XHI = 98304, XLO = 114688;  // X^T hi / lo, r0 and r1 [64 p][64 t] each
-    static constexpr int XW = 131072;                // weighted X^T, hi rows 0-63 / lo rows 64-127,
-                                                     // r0 and r1 [128][64 t] each; later fp32 scratch
+    static constexpr int XHI = 98304, XLO = 114688;  // X hi / lo [128 t][64 p] (MN-major operand)
+    static constexpr int XW = 131072;                // w x hi [128 t][64 p], then w x lo at XW + 16384
+                                                     // (MN-major operand); later fp32 scratch
     static constexpr int SHI = 163840, SLO = 172032; // S hi / lo [64 p][64 n]
     static constexpr int XR = 180224;                // raw x [131 t][64 p] bf16 (TMA, 128-byte swizzle)
     static constexpr int ZT = 197632;                // z [128 t][64 p] bf16 (TMA, 128-byte swizzle)
@@ -105,6 +109,19 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
 }
 
 // Four K-steps (K = 64) of D (+)= A B^T for K-major operands at shared addresses a, b.
+// Descriptor of an MN-major tile with 128-byte swizzling: rows of 128 bytes run along K, groups of
+// 8 rows are 1024 bytes apart (stride byte offset) and a second block of 64 M or N elements starts
+// `lbo` bytes after the first (leading byte offset).  A K-step of 16 rows advances it 2048 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // The descriptor's address field counts 16-byte units, so a 32-byte K-step adds 2 to it.
 __device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool first) {
     const uint64_t da = smem_desc_sw128(a), db = smem_desc_sw128(b);
@@ -330,20 +347,31 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 if (!wait(kXReady, c)) break;
                 tc_fence_after();
                 // dS^T = (w x)^T B: rows 0-63 from the hi part of w x, rows 64-127 from its lo part
-                for (int k = 0; k < 2; ++k)
-                    for (int r = 0; r < 2; ++r)
-                        mma_k64(tDS, sb + Smem::XW + r * 16384, sb + (k ? Smem::BTLO : Smem::BTHI) + r * 8192,
-                                kIdescN64, k == 0 && r == 0);
+                // (the MN-major A operand's two 64-row blocks), each times B hi + B lo
+                {
+                    const uint64_t da = smem_desc_sw128_mn(sb + Smem::XW, 16384);
+                    for (int k = 0; k < 2; ++k)
+                        for (int k16 = 0; k16 < kQ / 16; ++k16) {
+                            const uint64_t db = smem_desc_sw128(sb + (k ? Smem::BTLO : Smem::BTHI) + (k16 >> 2) * 8192 +
+                                                                32 * (k16 & 3));
+                            mma_bf16(tDS, da + (uint64_t)(2048 >> 4) * k16, db, kIdescN64_AMN, (k | k16) != 0);
+                        }
+                }
                 mma_commit(&bars[kBarD]);
                 ++nd;
                 if (!wait(kMReady, c)) break;
                 tc_fence_after();
-                for (int r = 0; r < 2; ++r)
-                    mma_k64(tYi, sb + Smem::MHI + r * 16384, sb + Smem::XHI + r * 8192, kIdescN64, r == 0);
-                for (int r = 0; r < 2; ++r)
-                    mma_k64(tYi, sb + Smem::MHI + r * 16384, sb + Smem::XLO + r * 8192, kIdescN64, false);
-                for (int r = 0; r < 2; ++r)
-                    mma_k64(tYi, sb + Smem::MLO + r * 16384, sb + Smem::XHI + r * 8192, kIdescN64, false);
+                // Y_intra = M X: A = M (K-major, two 64-column regions), B = X (MN-major [t][p])
+                {
+                    const uint32_t pa[3] = {Smem::MHI, Smem::MHI, Smem::MLO}, pb[3] = {Smem::XHI, Smem::XLO, Smem::XHI};
+                    for (int u = 0; u < 3; ++u) {
+                        const uint64_t db = smem_desc_sw128_mn(sb + pb[u], 16384);
+                        for (int k16 = 0; k16 < kQ / 16; ++k16) {
+                            const uint64_t dA = smem_desc_sw128(sb + pa[u] + (k16 >> 2) * 16384 + 32 * (k16 & 3));
+                            mma_bf16(tYi, dA, db + (uint64_t)(2048 >> 4) * k16, kIdescN64_BMN, (u | k16) != 0);
+                        }
+                    }
+                }
                 mma_commit(&bars[kBarY]);
                 ++ny;
                 if (c + 1 < nch) {
@@ -413,8 +441,8 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             workers_sync();
             const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
             {
-                // x of token i, positions kCW cg .., written as X^T hi/lo and as the state-update
-                // operand w_i x_i (w_i = 2^(s_Q - s_i) delta_i): hi rows 0-63, lo rows 64-127
+                // x of token i, positions kCW cg .., written as X hi/lo and as the state-update
+                // operand w_i x_i (w_i = 2^(s_Q - s_i) delta_i), hi and lo tiles
                 float r[4][kCW];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -438,7 +466,7 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     }
                 }
                 const float wi = ex2(s_Q - s_i) * dl_i;
-                const int reg = i >> 6, col = i & 63;
+                float u[kCW];
 #pragma unroll
                 for (int e = 0; e < kCW; ++e) {
                     const int pp = kCW * cg + e;
@@ -447,14 +475,23 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     xc = fmaf(w[1], r[1][e], xc);
                     xc = fmaf(w[2], r[2][e], xc);
                     xc = fmaf(w[3], r[3][e], xc);
-                    const float u = silu_in<Tin_bf16>(xc);
-                    uint32_t hi, lo;
-                    split2(u, wi * u, hi, lo);           // (x, w x) hi pair and lo pair
-                    const uint32_t o1 = sw128(pp, col);
-                    *reinterpret_cast<uint16_t*>(sm + Smem::XHI + reg * 8192 + o1) = (uint16_t)hi;
-                    *reinterpret_cast<uint16_t*>(sm + Smem::XLO + reg * 8192 + o1) = (uint16_t)lo;
-                    *reinterpret_cast<uint16_t*>(sm + Smem::XW + reg * 16384 + o1) = (uint16_t)(hi >> 16);
-                    *reinterpret_cast<uint16_t*>(sm + Smem::XW + reg * 16384 + sw128(64 + pp, col)) = (uint16_t)(lo >> 16);
+                    u[e] = silu_in<Tin_bf16>(xc);
+                }
+                // row i (token) of X and of w x, positions kCW cg .. as 16-byte swizzled chunks
+#pragma unroll
+                for (int c8 = 0; c8 < kCW / 8; ++c8) {
+                    uint32_t xh[4], xl[4], wh[4], wl[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float a0 = u[8 * c8 + 2 * k], a1 = u[8 * c8 + 2 * k + 1];
+                        split2(a0, a1, xh[k], xl[k]);
+                        split2(wi * a0, wi * a1, wh[k], wl[k]);
+                    }
+                    const uint32_t off = sw128(i, kCW * cg + 8 * c8);
+                    *reinterpret_cast<uint4*>(sm + Smem::XHI + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+                    *reinterpret_cast<uint4*>(sm + Smem::XLO + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+                    *reinterpret_cast<uint4*>(sm + Smem::XW + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                    *reinterpret_cast<uint4*>(sm + Smem::XW + 16384 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -629,6 +666,12 @@ k_ssd_decode(const SsdDecodeArgs a) {
         if (tid == 0) atomicOr(a.status, 2u);
         return;
     }
+    // the 16 KB state of (slot, head) is requested first, so its latency overlaps the conv below
+    const int pp = tid >> 2, n0 = 16 * (tid & 3);
+    float4* sp = reinterpret_cast<float4*>(a.ssm_state + (((int64_t)slot * H + h) * kP + pp) * kNs + n0);
+    float4 st[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st[k] = sp[k];
     if (tid < 192) {
         const int seg = tid / 64, k = tid % 64;
         const int64_t c = seg == 0 ? h * (int64_t)kP + k : HP + (seg == 2 ? (int64_t)G * kNs : 0) + (int64_t)g * kNs + k;
@@ -650,13 +693,11 @@ k_ssd_decode(const SsdDecodeArgs a) {
     __syncthreads();
     const float dl = softplus_in<Tin>(to_f32(reinterpret_cast<const Tin*>(a.dt)[(int64_t)r * H + h]) + a.dt_bias[h]);
     const float dA = ex2(dl * a.A[h] * kLog2e);
-    const int pp = tid >> 2, n0 = 16 * (tid & 3);
-    float4* sp = reinterpret_cast<float4*>(a.ssm_state + (((int64_t)slot * H + h) * kP + pp) * kNs + n0);
     const float dx = dl * u[pp];
     float y = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        float4 s = sp[k];
+        float4 s = st[k];
         const float* Bn = u + 64 + n0 + 4 * k;
         const float* Cn = u + 128 + n0 + 4 * k;
         s.x = fmaf(dA, s.x, dx * Bn[0]);
