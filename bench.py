@@ -850,8 +850,8 @@ def run_profile_target(which: str):
     """Launch one kernel 4 times (3 warm-up + 1 to capture) for ncu: the prefill on the bench
     workload, the segmented prefill of a batch-1 row, the decode step at batch 256 x d_inner
     8192, q8 over P=4 bf16 [4096, 1, 4096], the out_proj partial of the Falcon-Mamba-like
-    rank (16384 x 4096 x 2048), or the SSD prefill of the Zamba2-2.7B-like layer (4 x 2048
-    tokens, 80 heads of 64, d_state 64, one group)."""
+    rank (16384 x 4096 x 2048), the SSD prefill of the Zamba2-2.7B-like layer (4 x 2048
+    tokens, 80 heads of 64, d_state 64, one group), or its decode step at batch 256."""
     import torch
     from selective_state_space_prefill_gb300 import build as ssm_build
     if not ssm_build.up_to_date():
@@ -890,6 +890,14 @@ def run_profile_target(which: str):
         for _ in range(4):
             ssm.ssd_prefill(inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G,
                             workspace=ws)
+    elif which == "ssd_decode":
+        from selective_state_space_prefill_gb300.inputs import make_ssd_inputs, make_ssd_states
+        B, H, G = 256, 80, 1
+        inp = make_ssd_inputs(B, 1, H, n_groups=G, seed=B, device=dev)
+        cs, ss = (t.to(dev) for t in make_ssd_states(B, H, 64, 64, inp.channels, seed=B))
+        xb, z, dt = inp.xBC[:, 0].contiguous(), inp.z[:, 0].contiguous(), inp.dt[:, 0].contiguous()
+        for _ in range(4):
+            ssm.ssd_decode_step(xb, z, dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G, cs, ss)
     elif which == "out_proj":
         from selective_state_space_prefill_gb300.inputs import make_out_proj_inputs
         y, W = make_out_proj_inputs(16384, 2048, 4096, seed=0, device=dev)
@@ -915,7 +923,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8", "out_proj", "ssd"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill_seg", "decode", "q8", "out_proj", "ssd", "ssd_decode"],
+                    default=None,
                     help="only launch one kernel 4 times (for an ncu capture) and exit")
     args = ap.parse_args()
     _set_workload(args.workload)
