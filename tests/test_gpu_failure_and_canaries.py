@@ -124,3 +124,53 @@ def test_q8_and_out_proj_write_only_their_outputs():
         ssm.out_proj_partial(y, W, out=o.view, block_amax=a.view)
         o.check(f"out_proj {out_dtype}")
         a.check("out_proj block maxima")
+
+
+def _guards_intact(g, what):
+    torch.cuda.synchronize()
+    b = g.buf.cpu()
+    bits = torch.int16 if b.dtype == torch.bfloat16 else torch.int32
+    sentinel = torch.full((GUARD,), g.fill, dtype=b.dtype).view(bits)
+    assert torch.equal(b[:GUARD].view(bits), sentinel) and torch.equal(b[-GUARD:].view(bits), sentinel), \
+        f"{what}: a guard band was written"
+
+
+def test_ssd_prefill_writes_only_its_outputs():
+    from selective_state_space_prefill_gb300.inputs import make_ssd_inputs
+    batch, L, H, G = 2, 300, 4, 2
+    inp = make_ssd_inputs(batch, L, H, n_groups=G, seed=7).to(DEV)
+    need = ssm.ssd_prefill_workspace_bytes(batch, L, G)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        out = Guarded((batch, L, 64 * H), out_dtype, float("nan"))
+        cs = Guarded((batch, 3, inp.channels), torch.float32, float("nan"))
+        ss = Guarded((batch, H, 64, 64), torch.float32, float("nan"))
+        ws = Guarded((need // 4,), torch.float32, float("nan"))
+        ssm.ssd_prefill(inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G,
+                        out=out.view, conv_state_out=cs.view, ssm_state_out=ss.view,
+                        workspace=ws.view.view(torch.uint8))
+        for g, w in ((out, "out"), (cs, "conv_state_out"), (ss, "ssm_state_out")):
+            g.check(f"ssd_prefill {out_dtype} {w}")
+        # the workspace's token padding of the transposed planes is never written: guards only
+        _guards_intact(ws, f"ssd_prefill {out_dtype} workspace")
+
+
+def test_ssd_decode_writes_only_its_outputs():
+    from selective_state_space_prefill_gb300.inputs import make_ssd_inputs, make_ssd_states
+    batch, H, G, n_slots = 3, 4, 2, 5
+    inp = make_ssd_inputs(batch, 1, H, n_groups=G, seed=8).to(DEV)
+    cs0, ss0 = make_ssd_states(n_slots, H, 64, 64, inp.channels, seed=9)
+    fill = 12345.0
+    cs = Guarded(tuple(cs0.shape), torch.float32, fill)
+    ss = Guarded(tuple(ss0.shape), torch.float32, fill)
+    cs.view.copy_(cs0.to(DEV))
+    ss.view.copy_(ss0.to(DEV))
+    out = Guarded((batch, 64 * H), torch.float32, float("nan"))
+    slots = torch.tensor([4, 0, 2], dtype=torch.int32, device=DEV)
+    ssm.ssd_decode_step(inp.xBC[:, 0].contiguous(), inp.z[:, 0].contiguous(), inp.dt[:, 0].contiguous(),
+                        inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G, cs.view, ss.view,
+                        state_slot=slots, out=out.view)
+    out.check("ssd_decode_step out")
+    _guards_intact(cs, "ssd_decode_step conv_state")
+    _guards_intact(ss, "ssd_decode_step ssm_state")
+    for s in (1, 3):
+        assert torch.equal(cs.view[s].cpu(), cs0[s]) and torch.equal(ss.view[s].cpu(), ss0[s])

@@ -169,3 +169,16 @@ def test_ssd_decode_slots():
     assert_rms_close(gss[slots], ref["ssm_state"], TOL, "slot state")
     for s in (1, 3, 5):
         assert torch.equal(gss[s].cpu(), ss[s]) and torch.equal(gcs[s].cpu(), cs[s])
+
+
+def test_ssd_long_row():
+    """A long row (547 chunks, ragged end): the on-chip state carried through every chunk stays
+    within the bar against the oracle, output and final state."""
+    inp = make_ssd_inputs(1, 70000, 2, n_groups=1, seed=71)
+    out, cso, sso = _gpu(inp)
+    torch.cuda.synchronize()
+    ref = _oracle(inp)
+    e_out = assert_rms_close(out, ref["out"], TOL, "long row out")
+    e_st = assert_rms_close(sso, ref["ssm_state"], TOL, "long row state")
+    assert np.array_equal(cso.cpu().double().numpy(), ref["conv_state"])
+    print(f"long row: out {e_out:.2e} state {e_st:.2e}")
