@@ -220,7 +220,7 @@ template <typename Tout>
 __global__ void __launch_bounds__(kThAll, 1)
 k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
             const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ CUtensorMap tm_bt,
-            const SsdArgs p) {
+            const __grid_constant__ CUtensorMap tm_out, const SsdArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* s_cw = reinterpret_cast<float*>(sm + Smem::CW);
@@ -405,15 +405,17 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[k]);
         };
-        float dt_next = (cg == 0 && i < L) ? to_f32(dtp[(int64_t)i * p.dt_stride_t]) : 0.f;
+        // dt of (the next chunk's) token i, loaded a chunk ahead and widened only when used
+        Tin_bf16 dt_next = (cg == 0 && i < L) ? dtp[(int64_t)i * p.dt_stride_t] : __float2bfloat16_rn(0.f);
         for (int c = 0; c < nch; ++c) {
             const int t0 = c * kQ;
             float* s_dl = s_dl2 + (c & 1) * kQ;
             float* s_cs = s_cs2 + (c & 1) * kQ;
-            const float dt_i = dt_next;
-            if (cg == 0 && c + 1 < nch && t0 + kQ + i < L) dt_next = to_f32(dtp[(int64_t)(t0 + kQ + i) * p.dt_stride_t]);
+            const float dt_i = to_f32(dt_next);
+            if (cg == 0 && c + 1 < nch && t0 + kQ + i < L) dt_next = dtp[(int64_t)(t0 + kQ + i) * p.dt_stride_t];
 
             // ---- 2. delta, s (chunk-local cumulative delta A, log2 units), conv + SiLU of x
+            if (tid == 0) bulk_wait_read();          // the previous chunk's output tile has left X
             wait(kBarA, c);
             if (cg == 0) {
                 const int t = t0 + i;
@@ -586,7 +588,6 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 tmem_ld16(tYi + ((uint32_t)(32 * q) << 16) + (uint32_t)(kCW * cg), yi);
                 tmem_ld16(tYe + ((uint32_t)(32 * q) << 16) + (uint32_t)(kCW * cg), ye);
                 const float ei = ex2(s_i);
-                const int t = t0 + i;
                 float o[kCW];
 #pragma unroll
                 for (int e = 0; e < kCW / 8; ++e) {
@@ -600,28 +601,40 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         o[k + 1] = fmaf(ei, ye[k + 1], yi[k + 1]) * silu_in<Tin_bf16>(z1);
                     }
                 }
-                if (t < L && !bad) {
-                    Tout* dst = reinterpret_cast<Tout*>(p.out) + (int64_t)b * p.out_stride_b + (int64_t)t * p.out_stride_t +
-                                (int64_t)h * kP + kCW * cg;
-                    if constexpr (sizeof(Tout) == 4) {
+                // the tile row goes to shared memory over X (consumed by Y_intra), 128-byte swizzled,
+                // and leaves by one TMA store per 128-byte column block (rows past L are not written)
+                if constexpr (sizeof(Tout) == 4) {
+                    unsigned char* row = sm + Smem::XHI + (cg >> 1) * 16384 + i * 128;
 #pragma unroll
-                        for (int k = 0; k < kCW / 4; ++k)
-                            reinterpret_cast<float4*>(dst)[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                    } else {
+                    for (int k = 0; k < kCW / 4; ++k)
+                        *reinterpret_cast<float4*>(row + ((((cg & 1) * (kCW / 4) + k) ^ (i & 7)) << 4)) =
+                            make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                } else {
+                    unsigned char* row = sm + Smem::XHI + i * 128;
 #pragma unroll
-                        for (int k = 0; k < kCW / 8; ++k) {
-                            uint32_t w4[4];
+                    for (int k = 0; k < kCW / 8; ++k) {
+                        uint32_t w4[4];
 #pragma unroll
-                            for (int f = 0; f < 4; ++f)
-                                w4[f] = pack2(__float2bfloat16_rn(o[8 * k + 2 * f]), __float2bfloat16_rn(o[8 * k + 2 * f + 1]));
-                            reinterpret_cast<uint4*>(dst)[k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
+                        for (int f = 0; f < 4; ++f)
+                            w4[f] = pack2(__float2bfloat16_rn(o[8 * k + 2 * f]), __float2bfloat16_rn(o[8 * k + 2 * f + 1]));
+                        *reinterpret_cast<uint4*>(row + ((((kCW / 8) * cg + k) ^ (i & 7)) << 4)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
+            }
+            fence_proxy_async_smem();
+            workers_sync();
+            if (tid == 0 && !bad) {
+                constexpr int kBoxes = sizeof(Tout) == 4 ? 2 : 1;
+#pragma unroll
+                for (int k = 0; k < kBoxes; ++k)
+                    tma_store_3d(&tm_out, sm + Smem::XHI + k * 16384, h * kP + k * (kP / kBoxes), t0, b);
+                bulk_commit();
             }
             tc_fence_before();
             arrive(kDone);
         }
+        if (tid == 0) bulk_wait_read();              // the last output tile has left shared memory
         if (bad) {
             if (tid == 0) atomicOr(p.status, 1u);
         } else {
@@ -737,16 +750,17 @@ k_ssd_decode_shift(const SsdDecodeArgs a) {
     }
 }
 
-// 3-D bf16 tensor map: dims {d0, d1, d2} (d0 innermost), byte strides {s1, s2}, box {b0, b1, 1}.
+// 3-D tensor map (bf16 unless f32): dims {d0, d1, d2} (d0 innermost), byte strides {s1, s2}, box {b0, b1, 1}.
 bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-               uint32_t b0, uint32_t b1, bool swizzle) {
+               uint32_t b0, uint32_t b1, bool swizzle, bool f32 = false) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {s1, s2};
     cuuint32_t box[3] = {b0, b1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+               dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -780,7 +794,7 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
         return -1;
     }
 
-    CUtensorMap mx, mz, mbc, mbt;
+    CUtensorMap mx, mz, mbc, mbt, mo;
     const uint64_t xs_b = a.batch > 1 ? (uint64_t)a.xbc_stride_b * 2 : (uint64_t)L * a.xbc_stride_t * 2;
     const uint64_t zs_b = a.batch > 1 ? (uint64_t)a.z_stride_b * 2 : (uint64_t)L * a.z_stride_t * 2;
     const unsigned char* ws = static_cast<const unsigned char*>(a.workspace);
@@ -792,7 +806,12 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
                    true) ||
         !make_map3(&mbc, ws, kNs, (uint64_t)L, (uint64_t)(4 * BG), kNs * 2, (uint64_t)L * kNs * 2, kNs, kQ, true) ||
         !make_map3(&mbt, ws + w.bt_off, (uint64_t)L, kNs, (uint64_t)(2 * BG), (uint64_t)w.lp * 2,
-                   (uint64_t)w.lp * kNs * 2, 64, kNs, true)) {
+                   (uint64_t)w.lp * kNs * 2, 64, kNs, true) ||
+        // the output leaves through TMA stores of 128-byte-wide boxes: 32 fp32 or 64 bf16 columns
+        !make_map3(&mo, a.out, (uint64_t)HP, (uint64_t)L, (uint64_t)a.batch, (uint64_t)a.out_stride_t * (out_bf16 ? 2 : 4),
+                   a.batch > 1 ? (uint64_t)a.out_stride_b * (out_bf16 ? 2 : 4)
+                               : (uint64_t)L * a.out_stride_t * (out_bf16 ? 2 : 4),
+                   out_bf16 ? 64 : 32, kQ, true, !out_bf16)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
         return -1;
     }
@@ -811,7 +830,7 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
         }
         __atomic_fetch_or(&done[out_bf16], bit, __ATOMIC_ACQ_REL);
     }
-    kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kThAll, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, a);
+    kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kThAll, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, mo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);

@@ -182,3 +182,17 @@ def test_ssd_long_row():
     e_st = assert_rms_close(sso, ref["ssm_state"], TOL, "long row state")
     assert np.array_equal(cso.cpu().double().numpy(), ref["conv_state"])
     print(f"long row: out {e_out:.2e} state {e_st:.2e}")
+
+
+def test_ssd_short_prefills_chain():
+    """Prefills shorter than the conv window (2 tokens, then 1) splice the incoming conv state into
+    the outgoing one; a chain 2 + 1 + 200 equals one prefill of 203 tokens."""
+    inp = make_ssd_inputs(2, 203, 4, n_groups=2, seed=81)
+    ref = _oracle(inp)
+    o1, c1, s1 = _gpu(inp.token_slice(0, 2))
+    o2, c2, s2 = _gpu(inp.token_slice(2, 3), c1, s1)
+    o3, c3, s3 = _gpu(inp.token_slice(3, 203), c2, s2)
+    torch.cuda.synchronize()
+    assert_rms_close(torch.cat([o1, o2, o3], 1), ref["out"], TOL, "short chain out")
+    assert_rms_close(s3, ref["ssm_state"], TOL, "short chain state")
+    assert np.array_equal(c3.cpu().double().numpy(), ref["conv_state"])
