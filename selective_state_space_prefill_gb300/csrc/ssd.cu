@@ -63,6 +63,7 @@ constexpr uint32_t kIdescN64 = (1u << 4) | (1u << 7) | (1u << 10) | (8u << 17) |
 // elements contiguous in each 128-byte row
 constexpr uint32_t kIdescN64_AMN = kIdescN64 | (1u << 15);
 constexpr uint32_t kIdescN64_BMN = kIdescN64 | (1u << 16);
+constexpr uint32_t kIdescN128_BMN = kIdescN128 | (1u << 16);
 
 // Shared memory of k_ssd_chunk (byte offsets from a 1024-aligned base).  Operand tiles are
 // K-major rows of 64 bf16 (128 bytes) in 128-byte-swizzle atoms; a K extent of 128 is two such
@@ -294,7 +295,9 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *slot;
-    const uint32_t tG = tmem, tYi = tmem + 128, tYe = tmem + 192, tDS = tmem + 256;
+    // accumulators: G (128 columns), Y_intra and Y_inter (128 each: the hi*hi (+ lo*hi) products in
+    // columns 0-63, the hi*lo products in 64-127), dS^T (64)
+    const uint32_t tG = tmem, tYi = tmem + 128, tYe = tmem + 256, tDS = tmem + 384;
 
     if (producer) {
         if (lane == 0) {
@@ -339,8 +342,9 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 mma_k64(tG, sb + Smem::CHI, sb + Smem::BHI, kIdescN128, true);
                 mma_k64(tG, sb + Smem::CHI, sb + Smem::BLO, kIdescN128, false);
                 mma_k64(tG, sb + Smem::CLO, sb + Smem::BHI, kIdescN128, false);
-                mma_k64(tYe, sb + Smem::CHI, sb + Smem::SHI, kIdescN64, true);
-                mma_k64(tYe, sb + Smem::CHI, sb + Smem::SLO, kIdescN64, false);
+                // Y_inter: C hi against S hi and S lo stacked along N (the two tiles are adjacent),
+                // then C lo against S hi into the first half
+                mma_k64(tYe, sb + Smem::CHI, sb + Smem::SHI, kIdescN128, true);
                 mma_k64(tYe, sb + Smem::CLO, sb + Smem::SHI, kIdescN64, false);
                 mma_commit(&bars[kBarG]);
                 ++ng;
@@ -350,7 +354,9 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 // (the MN-major A operand's two 64-row blocks), each times B hi + B lo
                 {
                     const uint64_t da = smem_desc_sw128_mn(sb + Smem::XW, 16384);
+#pragma unroll
                     for (int k = 0; k < 2; ++k)
+#pragma unroll
                         for (int k16 = 0; k16 < kQ / 16; ++k16) {
                             const uint64_t db = smem_desc_sw128(sb + (k ? Smem::BTLO : Smem::BTHI) + (k16 >> 2) * 8192 +
                                                                 32 * (k16 & 3));
@@ -361,15 +367,21 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 ++nd;
                 if (!wait(kMReady, c)) break;
                 tc_fence_after();
-                // Y_intra = M X: A = M (K-major, two 64-column regions), B = X (MN-major [t][p])
+                // Y_intra = M X: A = M (K-major, two 64-column regions); B = X (MN-major [t][p]).
+                // M hi runs against X hi and X lo stacked along N (the X lo tile is the second
+                // 64-wide MN block, 16 KB on), M lo against X hi into the first half.
                 {
-                    const uint32_t pa[3] = {Smem::MHI, Smem::MHI, Smem::MLO}, pb[3] = {Smem::XHI, Smem::XLO, Smem::XHI};
-                    for (int u = 0; u < 3; ++u) {
-                        const uint64_t db = smem_desc_sw128_mn(sb + pb[u], 16384);
-                        for (int k16 = 0; k16 < kQ / 16; ++k16) {
-                            const uint64_t dA = smem_desc_sw128(sb + pa[u] + (k16 >> 2) * 16384 + 32 * (k16 & 3));
-                            mma_bf16(tYi, dA, db + (uint64_t)(2048 >> 4) * k16, kIdescN64_BMN, (u | k16) != 0);
-                        }
+                    const uint64_t dxx = smem_desc_sw128_mn(sb + Smem::XHI, 16384);
+                    const uint64_t dmh = smem_desc_sw128(sb + Smem::MHI), dml = smem_desc_sw128(sb + Smem::MLO);
+#pragma unroll
+                    for (int k16 = 0; k16 < kQ / 16; ++k16) {
+                        const uint64_t ka = (uint64_t)((k16 >> 2) * (16384 >> 4) + 2 * (k16 & 3));
+                        mma_bf16(tYi, dmh + ka, dxx + (uint64_t)(2048 >> 4) * k16, kIdescN128_BMN, k16 != 0);
+                    }
+#pragma unroll
+                    for (int k16 = 0; k16 < kQ / 16; ++k16) {
+                        const uint64_t ka = (uint64_t)((k16 >> 2) * (16384 >> 4) + 2 * (k16 & 3));
+                        mma_bf16(tYi, dml + ka, dxx + (uint64_t)(2048 >> 4) * k16, kIdescN64_BMN, true);
                     }
                 }
                 mma_commit(&bars[kBarY]);
@@ -584,9 +596,16 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             wait(kBarZ, c);
             tc_fence_after();
             {
-                float yi[kCW], ye[kCW];
-                tmem_ld16(tYi + ((uint32_t)(32 * q) << 16) + (uint32_t)(kCW * cg), yi);
-                tmem_ld16(tYe + ((uint32_t)(32 * q) << 16) + (uint32_t)(kCW * cg), ye);
+                float yi[kCW], ye[kCW], y2[kCW];
+                const uint32_t lanes = (uint32_t)(32 * q) << 16;
+                tmem_ld16(tYi + lanes + (uint32_t)(kCW * cg), yi);
+                tmem_ld16(tYi + lanes + (uint32_t)(64 + kCW * cg), y2);
+#pragma unroll
+                for (int k = 0; k < kCW; ++k) yi[k] += y2[k];
+                tmem_ld16(tYe + lanes + (uint32_t)(kCW * cg), ye);
+                tmem_ld16(tYe + lanes + (uint32_t)(64 + kCW * cg), y2);
+#pragma unroll
+                for (int k = 0; k < kCW; ++k) ye[k] += y2[k];
                 const float ei = ex2(s_i);
                 float o[kCW];
 #pragma unroll
