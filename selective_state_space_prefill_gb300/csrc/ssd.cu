@@ -417,22 +417,14 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[k]);
         };
-        // dt of (the next chunk's) token i, loaded a chunk ahead and widened only when used
-        Tin_bf16 dt_next = (cg == 0 && i < L) ? dtp[(int64_t)i * p.dt_stride_t] : __float2bfloat16_rn(0.f);
-        for (int c = 0; c < nch; ++c) {
-            const int t0 = c * kQ;
-            float* s_dl = s_dl2 + (c & 1) * kQ;
-            float* s_cs = s_cs2 + (c & 1) * kQ;
-            const float dt_i = to_f32(dt_next);
-            if (cg == 0 && c + 1 < nch && t0 + kQ + i < L) dt_next = dtp[(int64_t)(t0 + kQ + i) * p.dt_stride_t];
-
-            // ---- 2. delta, s (chunk-local cumulative delta A, log2 units), conv + SiLU of x
-            if (tid == 0) bulk_wait_read();          // the previous chunk's output tile has left X
-            wait(kBarA, c);
+        // delta and s (the chunk-local cumulative delta A, in log2 units) of chunk cc, into the
+        // parity buffers; returns (for every worker alike) whether any worker has seen an error
+        auto scan = [&](int cc, float dtv) -> bool {
+            float* sdl = s_dl2 + (cc & 1) * kQ;
+            float* scs = s_cs2 + (cc & 1) * kQ;
             if (cg == 0) {
-                const int t = t0 + i;
                 float dl = 0.f;
-                if (t < L) dl = softplus_in<Tin_bf16>(dt_i + bias);
+                if (cc * kQ + i < L) dl = softplus_in<Tin_bf16>(dtv + bias);
                 float v = dl * A2;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -440,20 +432,31 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     if (lane >= o) v += u;
                 }
                 if (lane == 31) s_ws[q] = v;
-                s_dl[i] = dl;
-                s_cs[i] = v;
+                sdl[i] = dl;
+                scs[i] = v;
             }
-            if (workers_any(bad)) {
-                bad = true;
-                break;
-            }
+            const bool any = workers_any(bad);
             if (cg == 0) {
                 float off = 0.f;
                 for (int k = 0; k < q; ++k) off += s_ws[k];
-                s_cs[i] += off;
+                scs[i] += off;
             }
             workers_sync();
+            return any;
+        };
+        const bool bad0 = scan(0, (cg == 0 && i < L) ? to_f32(dtp[(int64_t)i * p.dt_stride_t]) : 0.f);
+        bad = bad0;
+        for (int c = 0; c < nch && !bad0; ++c) {
+            const int t0 = c * kQ;
+            float* s_dl = s_dl2 + (c & 1) * kQ;
+            float* s_cs = s_cs2 + (c & 1) * kQ;
+            // dt of token i of the next chunk, for its scan during this one
+            const Tin_bf16 dt_n = (cg == 0 && c + 1 < nch && t0 + kQ + i < L) ? dtp[(int64_t)(t0 + kQ + i) * p.dt_stride_t]
+                                                                               : __float2bfloat16_rn(0.f);
             const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
+
+            // ---- 2. conv + SiLU of x (the chunk's delta and s were scanned during the previous one)
+            wait(kBarA, c);
             {
                 // x of token i, positions kCW cg .., written as X hi/lo and as the state-update
                 // operand w_i x_i (w_i = 2^(s_Q - s_i) delta_i), hi and lo tiles
@@ -491,6 +494,9 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     xc = fmaf(w[3], r[3][e], xc);
                     u[e] = silu_in<Tin_bf16>(xc);
                 }
+                // X is free once the previous chunk's output tile, staged there, has been read by its store
+                if (tid == 0) bulk_wait_read();
+                workers_sync();
                 // row i (token) of X and of w x, positions kCW cg .. as 16-byte swizzled chunks
 #pragma unroll
                 for (int c8 = 0; c8 < kCW / 8; ++c8) {
@@ -590,6 +596,12 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 }
             }
             fence_proxy_async_smem();
+
+            // ---- the next chunk's delta and s, while Y_intra runs
+            if (c + 1 < nch && scan(c + 1, to_f32(dt_n))) {
+                bad = true;
+                break;
+            }
 
             // ---- 5. out = (Y_intra + 2^(s_i) Y_inter) SiLU(z)   (Y_intra holds D x through M's diagonal)
             wait(kBarY, c);
