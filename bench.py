@@ -584,7 +584,7 @@ def bench_ssd(ssm, dev, stream, hbm_peak, flush, tc_peak):
         out = torch.empty(B, L, 64 * H, device=dev)
         cso = torch.empty(B, 3, inp.channels, device=dev)
         sso = torch.empty(B, H, 64, 64, device=dev)
-        ws = torch.empty(ssm.ssd_prefill_workspace_bytes(B, L, G), device=dev, dtype=torch.uint8)
+        ws = torch.empty(ssm.ssd_prefill_workspace_bytes(B, L, H, G), device=dev, dtype=torch.uint8)
         f = lambda: ssm.ssd_prefill(inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H,
                                     G, out=out, conv_state_out=cso, ssm_state_out=sso, workspace=ws, stream=stream)
         for _ in range(3):
@@ -886,7 +886,7 @@ def run_profile_target(which: str):
         from selective_state_space_prefill_gb300.inputs import make_ssd_inputs
         B, L, H, G = 4, 2048, 80, 1
         inp = make_ssd_inputs(B, L, H, n_groups=G, seed=0, device=dev)
-        ws = torch.empty(ssm.ssd_prefill_workspace_bytes(B, L, G), device=dev, dtype=torch.uint8)
+        ws = torch.empty(ssm.ssd_prefill_workspace_bytes(B, L, H, G), device=dev, dtype=torch.uint8)
         for _ in range(4):
             ssm.ssd_prefill(inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G,
                             workspace=ws)

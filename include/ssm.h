@@ -342,7 +342,7 @@ int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype,
  */
 
 /* Bytes of device workspace ssd_prefill needs for these sizes (0 on a bad size). */
-size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_groups);
+size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_heads, int n_groups);
 
 /*
  * ssd_prefill -- the SSD mixer over L tokens, on the tensor cores.  The recurrence is
@@ -368,9 +368,9 @@ size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_groups);
  *   conv_state_out, ssm_state_out  [batch][3][Cx] / [batch][H][64][64] float32, contiguous;
  *                            ssm_state_out 16-byte aligned
  *   workspace, workspace_bytes     device memory of at least
- *                            ssd_prefill_workspace_bytes(batch, seqlen, n_groups) bytes,
+ *                            ssd_prefill_workspace_bytes(batch, seqlen, n_heads, n_groups) bytes,
  *                            16-byte aligned, owned by the caller and not read afterwards
- * Asynchronous on cuda_stream (two kernels).  Returns SSM_OK or a negative status.
+ * Asynchronous on cuda_stream (three kernels).  Returns SSM_OK or a negative status.
  */
 int ssd_prefill(int batch, int seqlen, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
                 ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,

@@ -70,7 +70,7 @@ def load(path: Path | str | None = None):
     lib.ssm_out_proj_partial.restype = I
     lib.q8_reduce_partials.argtypes = [I, P, I, L, I, P, I, P, P, P]
     lib.q8_reduce_partials.restype = I
-    lib.ssd_prefill_workspace_bytes.argtypes = [I, I, I]
+    lib.ssd_prefill_workspace_bytes.argtypes = [I, I, I, I]
     lib.ssd_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_prefill.argtypes = [I, I, I, I, I, I, I, I, I, P, L, L, P, L, L, P, L, L, P, P, P, P, P, P, P,
                                 P, L, L, P, P, P, ctypes.c_size_t, P]
@@ -380,9 +380,9 @@ def _ssd_dims(n_heads, n_groups, head_dim=64, d_state=64):
     return n_heads * head_dim, n_heads * head_dim + 2 * n_groups * d_state
 
 
-def ssd_prefill_workspace_bytes(batch: int, seqlen: int, n_groups: int) -> int:
+def ssd_prefill_workspace_bytes(batch: int, seqlen: int, n_heads: int, n_groups: int) -> int:
     """ssd_prefill_workspace_bytes: device bytes ssd_prefill needs."""
-    return int(load().ssd_prefill_workspace_bytes(batch, seqlen, n_groups))
+    return int(load().ssd_prefill_workspace_bytes(batch, seqlen, n_heads, n_groups))
 
 
 def _ssd_params(conv_w, conv_b, A, D, dt_bias, H, Cx):
@@ -403,7 +403,7 @@ def ssd_prefill(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, n_heads, n_groups, co
                 workspace=None, stream=None):
     """ssd_prefill: xBC [batch, L, 64 H + 128 G], z [batch, L, 64 H], dt [batch, L, H] bf16
     (channel-stride-1 views), head_dim = d_state = 64.  ``workspace`` (a CUDA uint8 tensor of at
-    least ssd_prefill_workspace_bytes(...) bytes) is allocated here with torch when not given.
+    least ssd_prefill_workspace_bytes(batch, L, n_heads, n_groups) bytes) is allocated here with torch when not given.
     Returns (out [batch, L, 64 H], conv_state_out [batch, 3, Cx], ssm_state_out [batch, H, 64, 64])."""
     lib = load()
     _need_cuda(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, conv_state_in, ssm_state_in)
@@ -429,7 +429,7 @@ def ssd_prefill(xBC, z, dt, conv_w, conv_b, A, D, dt_bias, n_heads, n_groups, co
                     (conv_state_in, "conv_state_in", True), (ssm_state_in, "ssm_state_in", False)):
         if t is not None:
             _ssd_states(t, batch, H, Cx, n, c)
-    need = int(lib.ssd_prefill_workspace_bytes(batch, L, G))
+    need = int(lib.ssd_prefill_workspace_bytes(batch, L, H, G))
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
     _need_cuda(workspace)

@@ -192,7 +192,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
 
 extern "C" {
 
-int ssm_abi_version(void) { return 105; }
+int ssm_abi_version(void) { return 106; }
 
 const char* ssm_last_error(void) { return g_err; }
 
@@ -291,9 +291,11 @@ int ssm_out_proj_partial(int64_t M, int64_t N, int64_t K, const void* y, int64_t
     return SSM_OK;
 }
 
-size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_groups) {
-    if (batch < 1 || batch > 65535 || seqlen < 1 || seqlen > (1 << 30) || n_groups < 1 || n_groups > 65535) return 0;
-    return ssm::ssd_workspace_layout(batch, seqlen, n_groups).bytes;
+size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_heads, int n_groups) {
+    if (batch < 1 || batch > 65535 || seqlen < 1 || seqlen > (1 << 30) || n_heads < 1 || n_heads > 65535 ||
+        n_groups < 1 || n_heads % n_groups != 0)
+        return 0;
+    return ssm::ssd_workspace_layout(batch, seqlen, n_heads, n_groups).bytes;
 }
 
 int ssd_prefill(int batch, int seqlen, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
@@ -331,7 +333,7 @@ int ssd_prefill(int batch, int seqlen, int n_heads, int head_dim, int n_groups, 
         return fail(SSM_ERR_INVALID_ARG, "%s: a batch stride lets rows overlap", fn);
     if (batch > 1 && out_stride_b < (int64_t)(seqlen - 1) * out_stride_t + HP)
         return fail(SSM_ERR_INVALID_ARG, "%s: out_stride_b %lld lets batch rows overlap", fn, (long long)out_stride_b);
-    const size_t need = ssm::ssd_workspace_layout(batch, seqlen, n_groups).bytes;
+    const size_t need = ssm::ssd_workspace_layout(batch, seqlen, n_heads, n_groups).bytes;
     if (workspace_bytes < need)
         return fail(SSM_ERR_INVALID_ARG, "%s: workspace of %zu bytes given, %zu needed", fn, workspace_bytes, need);
     const int oe = esize(out_dtype);

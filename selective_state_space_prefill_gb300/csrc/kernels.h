@@ -88,18 +88,21 @@ struct SsdArgs {
     void* out;
     int64_t out_stride_b, out_stride_t;
     float *conv_state_out, *ssm_state_out;
-    void* workspace;                // B and C of every group after conv + SiLU, as bf16 hi/lo planes
-    int64_t ws_bt_off, ws_lp;       // filled in by launch_ssd_prefill
+    void* workspace;                // B and C of every group after conv + SiLU, as bf16 hi/lo planes,
+                                    // then delta and the chunk-local decay sums per head
+    int64_t ws_bt_off, ws_ds_off, ws_lp;   // filled in by launch_ssd_prefill
     unsigned int* status;
 };
 
 // Workspace of an SSD prefill: 4 planes [batch*G][L][64] (C hi, C lo, B hi, B lo), then at
-// bt_off 2 planes [batch*G][64][lp] (B hi, B lo, token-major), lp = L rounded up to 128.
+// bt_off 2 planes [batch*G][64][lp] (B hi, B lo, token-major), then at ds_off 2 fp32 planes
+// [batch*H][lp] (delta; s, the decay exponent summed from each 128-token chunk's start, in log2
+// units), lp = L rounded up to 128.
 struct SsdWorkspace {
     size_t bytes;
-    int64_t bt_off, lp;
+    int64_t bt_off, ds_off, lp;
 };
-SsdWorkspace ssd_workspace_layout(int batch, int seqlen, int n_groups);
+SsdWorkspace ssd_workspace_layout(int batch, int seqlen, int n_heads, int n_groups);
 
 // One-token SSD decode for a batch of requests, in place on the cached states of their slots.
 //   xBC [batch][Cx], z [batch][H*64], dt [batch][H] contiguous; conv_state [n_slots][3][Cx],

@@ -78,17 +78,16 @@ struct Smem {
     static constexpr int SHI = 163840, SLO = 172032; // S hi / lo [64 p][64 n]
     static constexpr int XR = 180224;                // raw x [131 t][64 p] bf16 (TMA, 128-byte swizzle)
     static constexpr int ZT = 197632;                // z [128 t][64 p] bf16 (TMA, 128-byte swizzle)
-    static constexpr int DL = 214016;                // delta [2][128] f32 (by chunk parity)
-    static constexpr int CS = DL + 1024;             // s (chunk-local cumulative delta*A) [2][128] f32
+    static constexpr int DL = 214016;                // delta [2][128] f32 (by chunk parity, TMA)
+    static constexpr int CS = DL + 1024;             // s (chunk-local cumulative delta*A) [2][128] f32 (TMA)
     static constexpr int CW = CS + 1024;             // conv weights of the head's x channels [64][4]
     static constexpr int CB = CW + 1024;             // conv bias [64]
-    static constexpr int WS = CB + 256;              // per-warp scan totals [4]
-    static constexpr int BAR = WS + 64;              // nine mbarriers (TMA, MMA groups, hand-offs)
+    static constexpr int BAR = CB + 256;             // nine mbarriers (TMA, MMA groups, hand-offs)
     static constexpr int SLOT = BAR + 80;            // TMEM base address, error flag
     static constexpr int TOTAL = SLOT + 16;
     static constexpr int ALLOC = TOTAL + 1024;       // + slack to align the base to 1024
     static constexpr int XR_BYTES = (kQ + 3) * kP * 2;
-    static constexpr int TX_A = XR_BYTES + 4 * 8192;     // raw x + B^T hi/lo
+    static constexpr int TX_A = XR_BYTES + 4 * 8192 + 2 * 512;   // raw x + B^T hi/lo + delta, s
     static constexpr int SCR_LD = 68;                    // fp32 scratch row stride (floats)
 };
 static_assert(Smem::XR + Smem::XR_BYTES <= Smem::ZT, "raw x tile overlaps z");
@@ -131,32 +130,53 @@ __device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, uint
 }
 
 // ------------------------------------------------------------------ pre-pass: B and C
-// grid (ceil(L / 64), G, batch), 256 threads: 64 tokens x 64 states of group g.
+// grid (ceil(L / 64), G, batch), 256 threads: 64 tokens x 64 states of group g.  The raw B and C
+// channels of the block's tokens and their 3-token halo are staged in shared memory with 16-byte
+// loads first; the conv then reads them from there.
 template <typename Tin>
 __global__ void __launch_bounds__(256)
 k_ssd_bc(const SsdArgs p) {
-    __shared__ __nv_bfloat16 tr[2][kNs][64 + 8];     // B hi / lo of the block, state-major
+    __shared__ __align__(16) __nv_bfloat16 raw_s[64 + 3][2][kNs];   // token row x (C, B) x state
+    __shared__ float hist[3][2][kNs];                                 // conv_state_in rows (first block)
+    __shared__ __nv_bfloat16 tr[2][kNs][64 + 8];                      // B hi / lo of the block, state-major
     const int t0 = blockIdx.x * 64, g = blockIdx.y, b = blockIdx.z;
     const int G = p.n_groups, BG = p.batch * G, bg = b * G + g, L = p.seqlen;
     const int64_t HP = (int64_t)p.n_heads * kP, Cx = HP + 2 * (int64_t)G * kNs;
     const Tin* xb = reinterpret_cast<const Tin*>(p.xBC) + (int64_t)b * p.xbc_stride_b;
     __nv_bfloat16* bc = reinterpret_cast<__nv_bfloat16*>(p.workspace);
     __nv_bfloat16* bt = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<unsigned char*>(p.workspace) + p.ws_bt_off);
-    auto raw = [&](int t, int64_t c) -> float {
-        if (t >= 0) return to_f32(xb[(int64_t)t * p.xbc_stride_t + c]);
-        return p.conv_state_in ? p.conv_state_in[((int64_t)b * 3 + 3 + t) * Cx + c] : 0.f;
+    auto chan = [&](int which, int n) -> int64_t {                    // 0: C, 1: B
+        return HP + (which ? 0 : (int64_t)G * kNs) + (int64_t)g * kNs + n;
+    };
+    // rows r = 0 .. 66 hold tokens t0 - 3 + r; 8 bf16 per 16-byte vector, 8 vectors per 64 states
+    for (int e = threadIdx.x; e < (64 + 3) * 2 * 8; e += 256) {
+        const int r = e / 16, which = (e / 8) & 1, v = e & 7, t = t0 - 3 + r;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (t >= 0 && t < L)
+            val = *reinterpret_cast<const uint4*>(xb + (int64_t)t * p.xbc_stride_t + chan(which, 8 * v));
+        *reinterpret_cast<uint4*>(&raw_s[r][which][8 * v]) = val;
+    }
+    if (t0 == 0 && threadIdx.x < 2 * kNs) {
+        const int which = threadIdx.x / kNs, n = threadIdx.x % kNs;
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+            hist[k][which][n] = p.conv_state_in ? p.conv_state_in[((int64_t)b * 3 + k) * Cx + chan(which, n)] : 0.f;
+    }
+    __syncthreads();
+    auto rawv = [&](int r, int which, int n) -> float {               // token t0 - 3 + r
+        return (t0 == 0 && r < 3) ? hist[r][which][n] : __bfloat162float(raw_s[r][which][n]);
     };
     for (int e = threadIdx.x; e < 64 * kNs; e += 256) {
         const int tl = e / kNs, n = e % kNs, t = t0 + tl;
         if (t >= L) continue;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {          // 0: C (planes 0, 1), 1: B (planes 2, 3)
-            const int64_t c = HP + (which ? 0 : (int64_t)G * kNs) + (int64_t)g * kNs + n;
+            const int64_t c = chan(which, n);
             const float4 w = *reinterpret_cast<const float4*>(p.conv_w + c * 4);
-            float xc = fmaf(w.x, raw(t - 3, c), p.conv_b[c]);
-            xc = fmaf(w.y, raw(t - 2, c), xc);
-            xc = fmaf(w.z, raw(t - 1, c), xc);
-            xc = fmaf(w.w, raw(t, c), xc);
+            float xc = fmaf(w.x, rawv(tl, which, n), p.conv_b[c]);
+            xc = fmaf(w.y, rawv(tl + 1, which, n), xc);
+            xc = fmaf(w.z, rawv(tl + 2, which, n), xc);
+            xc = fmaf(w.w, rawv(tl + 3, which, n), xc);
             __nv_bfloat16 hi, lo;
             split_bf16(silu_in<Tin>(xc), hi, lo);
             const int kind = which ? 2 : 0;
@@ -176,9 +196,59 @@ k_ssd_bc(const SsdArgs p) {
     // the conv window of the B and C channels after the last token
     if (blockIdx.x == gridDim.x - 1 && threadIdx.x < 2 * kNs) {
         const int which = threadIdx.x / kNs, n = threadIdx.x % kNs;
-        const int64_t c = HP + (which ? 0 : (int64_t)G * kNs) + (int64_t)g * kNs + n;
+        const int64_t c = chan(which, n);
 #pragma unroll
-        for (int k = 0; k < 3; ++k) p.conv_state_out[((int64_t)b * 3 + k) * Cx + c] = raw(L - 3 + k, c);
+        for (int k = 0; k < 3; ++k) {
+            const int t = L - 3 + k;
+            p.conv_state_out[((int64_t)b * 3 + k) * Cx + c] =
+                t >= 0 ? to_f32(xb[(int64_t)t * p.xbc_stride_t + c])
+                       : (p.conv_state_in ? p.conv_state_in[((int64_t)b * 3 + 3 + t) * Cx + c] : 0.f);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ pre-pass: delta and s
+// grid (lp / 128, batch, ceil(H / 32)), 128 threads: four lanes per head, each on 32 tokens of the
+// 128-token chunk: delta = softplus(dt + dt_bias) (0 past L) and s, the running sum of
+// delta A log2(e) from the chunk's start (constant past L); the four partial sums meet by shuffles.
+__global__ void __launch_bounds__(128)
+k_ssd_dt(const SsdArgs p) {
+    const int hq = threadIdx.x & 3, h = blockIdx.z * 32 + (threadIdx.x >> 2);
+    const bool live = h < p.n_heads;
+    const int b = blockIdx.y, t0 = blockIdx.x * kQ + 32 * hq, L = p.seqlen;
+    const int64_t BH = (int64_t)p.batch * p.n_heads;
+    const int hh = live ? h : 0;
+    const uint16_t* dtp = reinterpret_cast<const uint16_t*>(p.dt) + (int64_t)b * p.dt_stride_b + hh;
+    const float bias = p.dt_bias[hh], A2 = p.A[hh] * kLog2e;
+    uint16_t raw[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        raw[k] = 0;
+        if (live && t0 + k < L) raw[k] = dtp[(int64_t)(t0 + k) * p.dt_stride_t];
+    }
+    float d[32], s[32], run = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        d[k] = t0 + k < L ? softplus_in<Tin_bf16>(__uint_as_float((uint32_t)raw[k] << 16) + bias) : 0.f;
+        run = fmaf(d[k], A2, run);
+        s[k] = run;
+    }
+    // exclusive sum of the earlier quarters of the chunk
+    float inc = run;
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, inc, o, 4);
+        if (hq >= o) inc += u;
+    }
+    const float off = inc - run;
+    if (!live) return;
+    float4* dl = reinterpret_cast<float4*>(reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(p.workspace) +
+                                                                    p.ws_ds_off) + ((int64_t)b * p.n_heads + h) * p.ws_lp + t0);
+    float4* sc = dl + BH * p.ws_lp / 4;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        dl[k] = make_float4(d[4 * k], d[4 * k + 1], d[4 * k + 2], d[4 * k + 3]);
+        sc[k] = make_float4(s[4 * k] + off, s[4 * k + 1] + off, s[4 * k + 2] + off, s[4 * k + 3] + off);
     }
 }
 
@@ -221,12 +291,12 @@ template <typename Tout>
 __global__ void __launch_bounds__(kThAll, 1)
 k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
             const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ CUtensorMap tm_bt,
-            const __grid_constant__ CUtensorMap tm_out, const SsdArgs p) {
+            const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_ds,
+            const SsdArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* s_cw = reinterpret_cast<float*>(sm + Smem::CW);
     float* s_cb = reinterpret_cast<float*>(sm + Smem::CB);
-    float* s_ws = reinterpret_cast<float*>(sm + Smem::WS);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::BAR);
     // TMA groups (raw x + B^T, C/B tiles, z), MMA groups (G + Y_inter, dS, Y_intra), hand-offs
     enum { kBarA = 0, kBarB, kBarZ, kBarG, kBarD, kBarY, kXReady, kMReady, kDone, NBAR };
@@ -243,8 +313,7 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int g = h / (H / G), BG = p.batch * G, bg = b * G + g;
     const int64_t HP = (int64_t)H * kP, Cx = HP + 2 * (int64_t)G * kNs;
     const int nch = (L + kQ - 1) / kQ;
-    const float A2 = p.A[h] * kLog2e, bias = p.dt_bias[h], Dh = p.Dskip[h];
-    const Tin_bf16* dtp = reinterpret_cast<const Tin_bf16*>(p.dt) + (int64_t)b * p.dt_stride_b + h;
+    const float Dh = p.Dskip[h];
 
     if (tid == 0) {
         for (int k = 0; k < NBAR; ++k) mbar_init(&bars[k], k >= kXReady ? kWorkers / 32 : 1);
@@ -305,6 +374,9 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 const int t0 = c * kQ;
                 mbar_arrive_expect_tx(&bars[kBarA], Smem::TX_A);
                 tma_load_3d(sm + Smem::XR, &tm_x, &bars[kBarA], h * kP, t0 - 3, b);
+                // delta and s of the chunk into the parity buffers
+                tma_load_3d(sm + Smem::DL + (c & 1) * 512, &tm_ds, &bars[kBarA], t0, b * H + h, 0);
+                tma_load_3d(sm + Smem::CS + (c & 1) * 512, &tm_ds, &bars[kBarA], t0, (BG / G) * H + b * H + h, 0);
                 for (int k = 0; k < 2; ++k)
                     for (int r = 0; r < 2; ++r)
                         tma_load_3d(sm + (k ? Smem::BTLO : Smem::BTHI) + r * 8192, &tm_bt, &bars[kBarA],
@@ -417,46 +489,14 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[k]);
         };
-        // delta and s (the chunk-local cumulative delta A, in log2 units) of chunk cc, into the
-        // parity buffers; returns (for every worker alike) whether any worker has seen an error
-        auto scan = [&](int cc, float dtv) -> bool {
-            float* sdl = s_dl2 + (cc & 1) * kQ;
-            float* scs = s_cs2 + (cc & 1) * kQ;
-            if (cg == 0) {
-                float dl = 0.f;
-                if (cc * kQ + i < L) dl = softplus_in<Tin_bf16>(dtv + bias);
-                float v = dl * A2;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float u = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += u;
-                }
-                if (lane == 31) s_ws[q] = v;
-                sdl[i] = dl;
-                scs[i] = v;
-            }
-            const bool any = workers_any(bad);
-            if (cg == 0) {
-                float off = 0.f;
-                for (int k = 0; k < q; ++k) off += s_ws[k];
-                scs[i] += off;
-            }
-            workers_sync();
-            return any;
-        };
-        const bool bad0 = scan(0, (cg == 0 && i < L) ? to_f32(dtp[(int64_t)i * p.dt_stride_t]) : 0.f);
-        bad = bad0;
-        for (int c = 0; c < nch && !bad0; ++c) {
+        for (int c = 0; c < nch; ++c) {
             const int t0 = c * kQ;
             float* s_dl = s_dl2 + (c & 1) * kQ;
             float* s_cs = s_cs2 + (c & 1) * kQ;
-            // dt of token i of the next chunk, for its scan during this one
-            const Tin_bf16 dt_n = (cg == 0 && c + 1 < nch && t0 + kQ + i < L) ? dtp[(int64_t)(t0 + kQ + i) * p.dt_stride_t]
-                                                                               : __float2bfloat16_rn(0.f);
-            const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
 
-            // ---- 2. conv + SiLU of x (the chunk's delta and s were scanned during the previous one)
+            // ---- 2. conv + SiLU of x (raw x, B^T, delta and s of the chunk landed together)
             wait(kBarA, c);
+            const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
             {
                 // x of token i, positions kCW cg .., written as X hi/lo and as the state-update
                 // operand w_i x_i (w_i = 2^(s_Q - s_i) delta_i), hi and lo tiles
@@ -494,9 +534,10 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     xc = fmaf(w[3], r[3][e], xc);
                     u[e] = silu_in<Tin_bf16>(xc);
                 }
-                // X is free once the previous chunk's output tile, staged there, has been read by its store
+                // X is free once the previous chunk's output tile, staged there, has been read by its
+                // store; this barrier also tells every worker whether any of them has seen an error
                 if (tid == 0) bulk_wait_read();
-                workers_sync();
+                if (workers_any(bad)) bad = true;
                 // row i (token) of X and of w x, positions kCW cg .. as 16-byte swizzled chunks
 #pragma unroll
                 for (int c8 = 0; c8 < kCW / 8; ++c8) {
@@ -596,12 +637,6 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 }
             }
             fence_proxy_async_smem();
-
-            // ---- the next chunk's delta and s, while Y_intra runs
-            if (c + 1 < nch && scan(c + 1, to_f32(dt_n))) {
-                bad = true;
-                break;
-            }
 
             // ---- 5. out = (Y_intra + 2^(s_i) Y_inter) SiLU(z)   (Y_intra holds D x through M's diagonal)
             wait(kBarY, c);
@@ -800,32 +835,36 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 }  // namespace
 
-SsdWorkspace ssd_workspace_layout(int batch, int seqlen, int n_groups) {
+SsdWorkspace ssd_workspace_layout(int batch, int seqlen, int n_heads, int n_groups) {
     SsdWorkspace w{};
-    const int64_t BG = (int64_t)batch * n_groups;
+    const int64_t BG = (int64_t)batch * n_groups, BH = (int64_t)batch * n_heads;
     w.lp = round_up(seqlen, kQ);
     w.bt_off = round_up(4 * BG * seqlen * kNs * 2, 256);
-    w.bytes = (size_t)(w.bt_off + 2 * BG * kNs * w.lp * 2);
+    w.ds_off = round_up(w.bt_off + 2 * BG * kNs * w.lp * 2, 256);
+    w.bytes = (size_t)(w.ds_off + 2 * BH * w.lp * 4);
     return w;
 }
 
 int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, const char** why) {
     SsdArgs a = a0;
-    const SsdWorkspace w = ssd_workspace_layout(a.batch, a.seqlen, a.n_groups);
+    const SsdWorkspace w = ssd_workspace_layout(a.batch, a.seqlen, a.n_heads, a.n_groups);
     a.ws_bt_off = w.bt_off;
+    a.ws_ds_off = w.ds_off;
     a.ws_lp = w.lp;
     const int64_t HP = (int64_t)a.n_heads * kP, Cx = HP + 2 * (int64_t)a.n_groups * kNs;
     const int64_t BG = (int64_t)a.batch * a.n_groups;
     const int L = a.seqlen;
 
     k_ssd_bc<Tin_bf16><<<dim3((unsigned)((L + 63) / 64), (unsigned)a.n_groups, (unsigned)a.batch), 256, 0, stream>>>(a);
+    k_ssd_dt<<<dim3((unsigned)(w.lp / kQ), (unsigned)a.batch, (unsigned)((a.n_heads + 31) / 32)), 128, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return -1;
     }
 
-    CUtensorMap mx, mz, mbc, mbt, mo;
+    CUtensorMap mx, mz, mbc, mbt, mo, mds;
+    const int64_t BH = (int64_t)a.batch * a.n_heads;
     const uint64_t xs_b = a.batch > 1 ? (uint64_t)a.xbc_stride_b * 2 : (uint64_t)L * a.xbc_stride_t * 2;
     const uint64_t zs_b = a.batch > 1 ? (uint64_t)a.z_stride_b * 2 : (uint64_t)L * a.z_stride_t * 2;
     const unsigned char* ws = static_cast<const unsigned char*>(a.workspace);
@@ -842,7 +881,10 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
         !make_map3(&mo, a.out, (uint64_t)HP, (uint64_t)L, (uint64_t)a.batch, (uint64_t)a.out_stride_t * (out_bf16 ? 2 : 4),
                    a.batch > 1 ? (uint64_t)a.out_stride_b * (out_bf16 ? 2 : 4)
                                : (uint64_t)L * a.out_stride_t * (out_bf16 ? 2 : 4),
-                   out_bf16 ? 64 : 32, kQ, true, !out_bf16)) {
+                   out_bf16 ? 64 : 32, kQ, true, !out_bf16) ||
+        // delta and s planes [2 B H][lp] fp32, 128-token rows
+        !make_map3(&mds, ws + w.ds_off, (uint64_t)w.lp, (uint64_t)(2 * BH), 1, (uint64_t)w.lp * 4,
+                   (uint64_t)w.lp * 4 * 2 * BH, kQ, 1, false, true)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
         return -1;
     }
@@ -861,7 +903,7 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
         }
         __atomic_fetch_or(&done[out_bf16], bit, __ATOMIC_ACQ_REL);
     }
-    kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kThAll, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, mo, a);
+    kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kThAll, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, mo, mds, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);

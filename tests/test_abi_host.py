@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding.EXPORTS)
     for fn in names:
         assert hasattr(lib, fn), fn
-    assert lib.ssm_abi_version() == 105
+    assert lib.ssm_abi_version() == 106
 
 
 FAKE = 0x10000  # 64 KiB-aligned fake device address, never dereferenced
@@ -211,10 +211,17 @@ def _ssd(lib, ws_bytes=1 << 30, **kw):
 
 
 def test_ssd_workspace_bytes(lib):
-    # 4 planes [B*G][L][64] + 2 planes [B*G][64][L rounded up to 128], bf16
-    assert lib.ssd_prefill_workspace_bytes(4, 2048, 1) == 4 * 4 * 2048 * 64 * 2 + 2 * 4 * 64 * 2048 * 2
-    assert lib.ssd_prefill_workspace_bytes(1, 300, 2) == 4 * 2 * 300 * 128 + 2 * 2 * 64 * 384 * 2
-    assert lib.ssd_prefill_workspace_bytes(0, 300, 2) == 0
+    # 4 bf16 planes [B*G][L][64], 2 bf16 planes [B*G][64][Lp], 2 fp32 planes [B*H][Lp]
+    # (Lp = L rounded up to 128; each part starts on a 256-byte boundary)
+    up = lambda v: (v + 255) // 256 * 256
+    a = up(4 * 4 * 2048 * 64 * 2)
+    b = up(a + 2 * 4 * 64 * 2048 * 2)
+    assert lib.ssd_prefill_workspace_bytes(4, 2048, 80, 1) == b + 2 * 4 * 80 * 2048 * 4
+    a = up(4 * 2 * 300 * 128)
+    b = up(a + 2 * 2 * 64 * 384 * 2)
+    assert lib.ssd_prefill_workspace_bytes(1, 300, 4, 2) == b + 2 * 4 * 384 * 4
+    assert lib.ssd_prefill_workspace_bytes(0, 300, 4, 2) == 0
+    assert lib.ssd_prefill_workspace_bytes(1, 300, 3, 2) == 0           # groups must divide heads
 
 
 @pytest.mark.parametrize("kw,code", [

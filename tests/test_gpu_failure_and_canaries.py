@@ -139,7 +139,7 @@ def test_ssd_prefill_writes_only_its_outputs():
     from selective_state_space_prefill_gb300.inputs import make_ssd_inputs
     batch, L, H, G = 2, 300, 4, 2
     inp = make_ssd_inputs(batch, L, H, n_groups=G, seed=7).to(DEV)
-    need = ssm.ssd_prefill_workspace_bytes(batch, L, G)
+    need = ssm.ssd_prefill_workspace_bytes(batch, L, H, G)
     for out_dtype in (torch.float32, torch.bfloat16):
         out = Guarded((batch, L, 64 * H), out_dtype, float("nan"))
         cs = Guarded((batch, 3, inp.channels), torch.float32, float("nan"))
