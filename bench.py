@@ -644,7 +644,7 @@ def bench_ssd(ssm, dev, stream, hbm_peak, flush, tc_peak):
         res[f"decode_b{batch}_h80"] = {"us_per_step": 1e6 * t, "steps_per_s": 1 / t, "GB_s": byts / t / 1e9,
                                        "frac_hbm": byts / t / 1e9 / hbm_peak}
         del g
-    res["note"] = ("k_ssd_bc (B, C conv + hi/lo planes) + k_ssd_chunk (tcgen05: G = C B^T, M X, C S^T and the "
+    res["note"] = ("k_ssd_pre (B, C conv + hi/lo planes, delta and decay sums) + k_ssd_chunk (tcgen05: G = C B^T, M X, C S^T and the "
                    "state update on bf16 hi/lo operand pairs, fp32 TMEM accumulators; a producer warp issues "
                    "TMA and MMA, 16 worker warps the arithmetic).  frac_hbm is against algorithmic bytes; "
                    "mma_TFLOP_s counts the hi/lo products the kernel issues (frac_tensor of the measured bf16 "

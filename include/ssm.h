@@ -370,7 +370,7 @@ size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_heads, int n_gro
  *   workspace, workspace_bytes     device memory of at least
  *                            ssd_prefill_workspace_bytes(batch, seqlen, n_heads, n_groups) bytes,
  *                            16-byte aligned, owned by the caller and not read afterwards
- * Asynchronous on cuda_stream (three kernels).  Returns SSM_OK or a negative status.
+ * Asynchronous on cuda_stream (two kernels).  Returns SSM_OK or a negative status.
  */
 int ssd_prefill(int batch, int seqlen, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
                 ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,

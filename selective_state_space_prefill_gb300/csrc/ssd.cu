@@ -24,9 +24,10 @@
 // hi*hi + hi*lo + lo*hi.
 //
 // Kernels:
-//   k_ssd_bc      (pre-pass) conv + SiLU of every group's B and C channels, written as hi/lo
+//   k_ssd_pre     (pre-pass) conv + SiLU of every group's B and C channels, written as hi/lo
 //                 planes [t][n] (the K-major operands of C B^T and C S^T) and, for B, also as
-//                 token-major planes [n][t] (the K-major operand of the state update).
+//                 token-major planes [n][t] (the K-major operand of the state update); and, in
+//                 the same launch, delta and the chunk-local decay sums of every head.
 //   k_ssd_chunk   one CTA per (batch row, head) walks the row's chunks in order, so the fp32
 //                 state stays on chip: TMA brings the raw x (with a 3-token conv halo), z and the
 //                 B/C tiles; the CTA's threads compute the x conv, the decays and the operands
@@ -130,16 +131,15 @@ __device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, uint
 }
 
 // ------------------------------------------------------------------ pre-pass: B and C
-// grid (ceil(L / 64), G, batch), 256 threads: 64 tokens x 64 states of group g.  The raw B and C
-// channels of the block's tokens and their 3-token halo are staged in shared memory with 16-byte
-// loads first; the conv then reads them from there.
+// One block of 256 threads: 64 tokens (block bx of nbx) x 64 states of group g of row b.  The raw
+// B and C channels of the block's tokens and their 3-token halo are staged in shared memory with
+// 16-byte loads first; the conv then reads them from there.
 template <typename Tin>
-__global__ void __launch_bounds__(256)
-k_ssd_bc(const SsdArgs p) {
+__device__ __forceinline__ void ssd_bc_block(const SsdArgs& p, int bx, int nbx, int g, int b) {
     __shared__ __align__(16) __nv_bfloat16 raw_s[64 + 3][2][kNs];   // token row x (C, B) x state
     __shared__ float hist[3][2][kNs];                                 // conv_state_in rows (first block)
     __shared__ __nv_bfloat16 tr[2][kNs][64 + 8];                      // B hi / lo of the block, state-major
-    const int t0 = blockIdx.x * 64, g = blockIdx.y, b = blockIdx.z;
+    const int t0 = bx * 64;
     const int G = p.n_groups, BG = p.batch * G, bg = b * G + g, L = p.seqlen;
     const int64_t HP = (int64_t)p.n_heads * kP, Cx = HP + 2 * (int64_t)G * kNs;
     const Tin* xb = reinterpret_cast<const Tin*>(p.xBC) + (int64_t)b * p.xbc_stride_b;
@@ -194,7 +194,7 @@ k_ssd_bc(const SsdArgs p) {
         if (t < L) bt[(((int64_t)k * BG + bg) * kNs + n) * p.ws_lp + t] = tr[k][n][tl];
     }
     // the conv window of the B and C channels after the last token
-    if (blockIdx.x == gridDim.x - 1 && threadIdx.x < 2 * kNs) {
+    if (bx == nbx - 1 && threadIdx.x < 2 * kNs) {
         const int which = threadIdx.x / kNs, n = threadIdx.x % kNs;
         const int64_t c = chan(which, n);
 #pragma unroll
@@ -208,14 +208,13 @@ k_ssd_bc(const SsdArgs p) {
 }
 
 // ------------------------------------------------------------------ pre-pass: delta and s
-// grid (lp / 128, batch, ceil(H / 32)), 128 threads: four lanes per head, each on 32 tokens of the
-// 128-token chunk: delta = softplus(dt + dt_bias) (0 past L) and s, the running sum of
-// delta A log2(e) from the chunk's start (constant past L); the four partial sums meet by shuffles.
-__global__ void __launch_bounds__(128)
-k_ssd_dt(const SsdArgs p) {
-    const int hq = threadIdx.x & 3, h = blockIdx.z * 32 + (threadIdx.x >> 2);
+// One block of 256 threads: chunk cx of row b, heads [64 hb, 64 hb + 64); four lanes per head, each
+// on 32 tokens of the 128-token chunk: delta = softplus(dt + dt_bias) (0 past L) and s, the running
+// sum of delta A log2(e) from the chunk's start (constant past L); the partial sums meet by shuffles.
+__device__ __forceinline__ void ssd_dt_block(const SsdArgs& p, int cx, int b, int hb) {
+    const int hq = threadIdx.x & 3, h = hb * 64 + (threadIdx.x >> 2);
     const bool live = h < p.n_heads;
-    const int b = blockIdx.y, t0 = blockIdx.x * kQ + 32 * hq, L = p.seqlen;
+    const int t0 = cx * kQ + 32 * hq, L = p.seqlen;
     const int64_t BH = (int64_t)p.batch * p.n_heads;
     const int hh = live ? h : 0;
     const uint16_t* dtp = reinterpret_cast<const uint16_t*>(p.dt) + (int64_t)b * p.dt_stride_b + hh;
@@ -249,6 +248,21 @@ k_ssd_dt(const SsdArgs p) {
     for (int k = 0; k < 8; ++k) {
         dl[k] = make_float4(d[4 * k], d[4 * k + 1], d[4 * k + 2], d[4 * k + 3]);
         sc[k] = make_float4(s[4 * k] + off, s[4 * k + 1] + off, s[4 * k + 2] + off, s[4 * k + 3] + off);
+    }
+}
+
+// Both pre-passes in one launch, so that they run side by side: blocks [0, n_bc) convolve B and C
+// (grid ceil(L / 64) x G x batch, flattened), the rest compute delta and s (lp / 128 x batch x
+// ceil(H / 64)).
+__global__ void __launch_bounds__(256)
+k_ssd_pre(const SsdArgs p, int nbx, int n_bc, int ncx) {
+    const int blk = blockIdx.x;
+    if (blk < n_bc) {
+        const int bx = blk % nbx, g = (blk / nbx) % p.n_groups, b = blk / (nbx * p.n_groups);
+        ssd_bc_block<Tin_bf16>(p, bx, nbx, g, b);
+    } else {
+        const int k = blk - n_bc;
+        ssd_dt_block(p, k % ncx, (k / ncx) % p.batch, k / (ncx * p.batch));
     }
 }
 
@@ -855,8 +869,16 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
     const int64_t BG = (int64_t)a.batch * a.n_groups;
     const int L = a.seqlen;
 
-    k_ssd_bc<Tin_bf16><<<dim3((unsigned)((L + 63) / 64), (unsigned)a.n_groups, (unsigned)a.batch), 256, 0, stream>>>(a);
-    k_ssd_dt<<<dim3((unsigned)(w.lp / kQ), (unsigned)a.batch, (unsigned)((a.n_heads + 31) / 32)), 128, 0, stream>>>(a);
+    {
+        const int nbx = (L + 63) / 64, ncx = (int)(w.lp / kQ);
+        const int64_t n_bc = (int64_t)nbx * a.n_groups * a.batch;
+        const int64_t n_dt = (int64_t)ncx * a.batch * ((a.n_heads + 63) / 64);
+        if (n_bc + n_dt > 0x7fffffffLL) {
+            *why = "too many pre-pass blocks";
+            return -1;
+        }
+        k_ssd_pre<<<(unsigned)(n_bc + n_dt), 256, 0, stream>>>(a, nbx, (int)n_bc, ncx);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
