@@ -29,11 +29,11 @@
 //                 token-major planes [n][t] (the K-major operand of the state update); and, in
 //                 the same launch, delta and the chunk-local decay sums of every head.
 //   k_ssd_chunk   one CTA per (batch row, head) walks the row's chunks in order, so the fp32
-//                 state stays on chip: TMA brings the raw x (with a 3-token conv halo), z and the
-//                 B/C tiles; the CTA's threads compute the x conv, the decays and the operands
-//                 they own (X, the state-update weights, M, S) into 128-byte-swizzled shared
-//                 memory; one thread issues the MMAs; the threads read the accumulators back
-//                 with tcgen05.ld.
+//                 state stays on chip: a producer warp brings the raw x (with a 3-token conv
+//                 halo), z, the B/C tiles and the chunk's delta and decay sums by TMA and issues
+//                 the MMAs; 16 worker warps compute the x conv and the operands they own (X, the
+//                 state-update weights, M, S) into 128-byte-swizzled shared memory, read the
+//                 accumulators back with tcgen05.ld, and send the output tile out by TMA stores.
 //   k_ssd_decode  one CTA per (request, head): the one-token recurrence on the cached state
 //                 [64 x 64] in place, then k_ssd_decode_shift moves the conv windows of the B
 //                 and C channels (shared by the heads of a group, so they move after every head
@@ -73,7 +73,8 @@ struct Smem {
     static constexpr int CHI = 0, CLO = 16384, BHI = 32768, BLO = 49152;  // [128 t][64 n] (TMA)
     static constexpr int MHI = 0, MLO = 32768;       // M hi / lo, r0 and r1 [128 i][64 j] each (over C, B)
     static constexpr int BTHI = 65536, BTLO = 81920; // B^T hi / lo, r0 and r1 [64 n][64 t] each (TMA)
-    static constexpr int XHI = 98304, XLO = 114688;  // X hi / lo [128 t][64 p] (MN-major operand)
+    static constexpr int XHI = 98304, XLO = 114688;  // X hi / lo [128 t][64 p] (MN-major operand); once
+                                                     // Y_intra has run, the output tile for the TMA store
     static constexpr int XW = 131072;                // w x hi [128 t][64 p], then w x lo at XW + 16384
                                                      // (MN-major operand); later fp32 scratch
     static constexpr int SHI = 163840, SLO = 172032; // S hi / lo [64 p][64 n]
@@ -271,12 +272,12 @@ k_ssd_pre(const SsdArgs p, int nbx, int n_bc, int ncx) {
 // lane) issues every TMA copy and tcgen05.mma.  A chunk runs in phases; the tensor cores work on
 // one group of products while the workers work on the next:
 //   workers                                         producer
-//   2. (raw x) delta, s, conv + SiLU -> X^T, w x     1. (C, B tiles; previous chunk done)
+//   2. (raw x, delta, s) conv + SiLU -> X, w x       1. (C, B tiles; previous chunk done)
 //      -> "X ready"                                     G = C B^T, Y_inter = C S_prev^T; z
 //   3. (G) M -> over the C, B tiles -> "M ready"     2. (X ready) dS^T = (w x)^T B
 //   4. (dS) S = 2^(s_Q) S + dS -> S tiles            3. (M ready) Y_intra = M X
-//   5. (Y_intra, z) out = (Y_intra + 2^(s_i) Y_inter) 4. (dS) refill raw x, B^T
-//      SiLU(z) -> "chunk done"                       5. (Y_intra) refill C, B
+//   5. (Y_intra, z) out = (Y_intra + 2^(s_i) Y_inter) 4. (dS) refill raw x, B^T, delta, s
+//      SiLU(z) -> over X -> TMA store -> "chunk done" 5. (Y_intra) refill C, B
 // Each TMA group, MMA group and hand-off completes its own mbarrier once per chunk.  Every wait
 // is bounded; a worker whose wait expires keeps walking the chunk without waiting and the error
 // is OR-reduced at the next worker barrier, so no warp is ever left waiting at a barrier.
