@@ -95,7 +95,7 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_s: float) -> float
 # DRAM bytes (read + write) of one k_prefill launch on the bench workload, from the ncu capture
 # summarised in profiles/k_prefill_mamba130m_like_b4_l2048_d1536.md, valid only for the prefill
 # source it was taken on (first 16 hex digits of its sha256); any other source reports null.
-PREFILL_NCU_TRAFFIC = {"bytes": 76209408 + 16988160, "prefill_cu_sha256_16": "4ec2f2a417d4917a"}
+PREFILL_NCU_TRAFFIC = {"bytes": 76212480 + 17341440, "prefill_cu_sha256_16": "cb4e88e1f264b8d0"}
 
 
 def _prefill_traffic():

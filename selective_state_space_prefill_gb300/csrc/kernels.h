@@ -25,6 +25,9 @@ struct PrefillArgs {
     // and the product of its decays.
     int seg_len, n_seg;
     float* ws;
+    // 1: the output leaves through TMA stores of [chunk x 16 channels] tiles staged in shared
+    // memory (needs a 16-byte-aligned output with 16-byte strides); 0: per-lane stores
+    int out_tma;
 };
 
 struct PrefillLaunch {

@@ -44,6 +44,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace ssm {
 
@@ -76,7 +77,9 @@ struct Layout {
     static constexpr int OFF_CF = OFF_BF + 2 * BCF;      // [2][TC][16]
     static constexpr int OFF_XCH = OFF_CF + 2 * BCF;     // [2 slots][S][32] float4
     static constexpr int XCH_BYTES = 2 * S * 32 * 16;
-    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    static constexpr int OFF_OUT = align128(OFF_XCH + XCH_BYTES);   // [2 parities][TC][16] output tiles
+    static constexpr int OUT_BYTES = 2 * TC * kCD * 4;
+    static constexpr int OFF_BAR = OFF_OUT + OUT_BYTES;
     static constexpr int TOTAL = OFF_BAR + kStages * 8;
 };
 
@@ -94,7 +97,8 @@ template <int S, int K, typename Tin, typename Tout, bool kSeg>
 __global__ void __launch_bounds__(S * 32, 3)
 k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_B,
-          const __grid_constant__ CUtensorMap tm_C, const PrefillArgs p) {
+          const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_out,
+          const PrefillArgs p) {
     using Lay = Layout<S, K, Tin>;
     constexpr int TC = Lay::TC;
     constexpr int KH = K / 2;            // tokens whose per-token work this lane does
@@ -103,6 +107,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     float* Bf0 = reinterpret_cast<float*>(smem + Lay::OFF_BF);
     float* Cf0 = reinterpret_cast<float*>(smem + Lay::OFF_CF);
     float4* xch = reinterpret_cast<float4*>(smem + Lay::OFF_XCH);
+    Tout* out_s = reinterpret_cast<Tout*>(smem + Lay::OFF_OUT);          // [2][TC][16]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::OFF_BAR);
 
     const int lane = threadIdx.x & 31;
@@ -214,8 +219,17 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 for (int j = it; j < n_iter && j < it + kStages - 1; ++j)
                     (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1),
                                             100000000ull);
+                bulk_wait_all();
             }
             return;
+        }
+        if (p.out_tma && it > 0 && threadIdx.x == 0) {
+            // the previous chunk's output tile (staged and fenced before this barrier) leaves by TMA;
+            // rows past L and channels past d_inner are outside the map and not written.  The tile
+            // written two chunks ago, in the buffer this chunk reuses, has then been read.
+            tma_store_3d(&tm_out, out_s + ((it - 1) & 1) * TC * kCD, d0, seg_first_token() + (it - 1) * TC, b);
+            bulk_commit();
+            bulk_wait_read_all_but_last();
         }
 
         // ---- per-token work for this lane's half of the warp's K tokens:
@@ -316,9 +330,24 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             if (dvalid && t < L) {
                 const float yv = (mine + other) + ud[k];
                 const float gz = silu_in<Tin>(to_f32(zs[(r0 + k) * kCD + c]));
-                reinterpret_cast<Tout*>(p.out)[(int64_t)b * p.out_stride_b + (int64_t)t * p.out_stride_t + d] =
-                    from_f32<Tout>(yv * gz);
+                if (p.out_tma)
+                    out_s[((it & 1) * TC + r0 + k) * kCD + c] = from_f32<Tout>(yv * gz);
+                else
+                    reinterpret_cast<Tout*>(p.out)[(int64_t)b * p.out_stride_b + (int64_t)t * p.out_stride_t + d] =
+                        from_f32<Tout>(yv * gz);
             }
+        }
+        if (p.out_tma) fence_proxy_async_smem();         // the tile is read by the next chunk's store
+    }
+    if (p.out_tma) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (n_iter > 0) {
+                tma_store_3d(&tm_out, out_s + ((n_iter - 1) & 1) * TC * kCD, d0,
+                             seg_first_token() + (n_iter - 1) * TC, b);
+                bulk_commit();
+            }
+            bulk_wait_all();
         }
     }
 
@@ -627,7 +656,7 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
     const uint64_t sb = (uint64_t)(q.batch > 1 ? a.in_stride_b : (int64_t)a.seqlen * a.in_stride_t) * es;
     const uint64_t st = (uint64_t)a.in_stride_t * es;
     const uint64_t bc_t = (uint64_t)kN * es, bc_b = (uint64_t)a.seqlen * kN * es;
-    CUtensorMap mx, mz, mdt, mB, mC;
+    CUtensorMap mx, mz, mdt, mB, mC, mo;
     if (!make_map(&mx, a.x, dt, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC + 3) ||
         !make_map(&mz, q.z, dt, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
         !make_map(&mdt, q.dt, dt, a.d_inner, a.seqlen, q.batch, st, sb, kCD, TC) ||
@@ -636,6 +665,17 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
         return -1;
     }
+    // the output leaves by TMA stores when its base and strides are 16-byte multiples
+    PrefillArgs ak = a;
+    const uint64_t eo = sizeof(Tout);
+    const uint64_t ot = (uint64_t)a.out_stride_t * eo;
+    const uint64_t ob = q.batch > 1 ? (uint64_t)a.out_stride_b * eo : (uint64_t)a.seqlen * ot;
+    ak.out_tma = (reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && ot % 16 == 0 && ob % 16 == 0) ? 1 : 0;
+    if (ak.out_tma &&
+        !make_map(&mo, a.out, sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  a.d_inner, a.seqlen, q.batch, ot, ob, kCD, TC))
+        ak.out_tma = 0;
+    if (!ak.out_tma) mo = mx;                        // not read
     const unsigned gx = (unsigned)((a.d_inner + kCD - 1) / kCD);
     if (a.n_seg > 1) {
         // pass A (segments 0 .. n_seg-2), then pass B
@@ -655,7 +695,7 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
     static unsigned long long attr_row = 0, attr_seg = 0;
     auto kern = a.n_seg > 1 ? k_prefill<S, K, Tin, Tout, true> : k_prefill<S, K, Tin, Tout, false>;
     if (!opt_in_smem(kern, Lay::TOTAL, a.n_seg > 1 ? &attr_seg : &attr_row, why)) return -1;
-    kern<<<dim3(gx, q.batch, a.n_seg), S * 32, Lay::TOTAL, stream>>>(mx, mz, mdt, mB, mC, a);
+    kern<<<dim3(gx, q.batch, a.n_seg), S * 32, Lay::TOTAL, stream>>>(mx, mz, mdt, mB, mC, mo, ak);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);

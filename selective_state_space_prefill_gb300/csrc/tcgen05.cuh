@@ -112,6 +112,12 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every bulk store this thread committed has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... every one but the most recently committed.
+__device__ __forceinline__ void bulk_wait_read_all_but_last() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Wait until every bulk store this thread committed has completed (its global writes included).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Order this thread's generic-proxy shared-memory writes before later async-proxy reads
 // (tcgen05.mma operands written by threads rather than by TMA).
