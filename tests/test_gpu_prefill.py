@@ -129,3 +129,22 @@ def test_prefill_fp32_seed_sweep(seg_len):
         ref = oracle_prefill(inp)
         assert_rel_close(out, ref["out"], 1e-5, f"out seed {seed}")
         assert_rel_close(sso, ref["ssm_state"], 1e-5, f"state seed {seed}")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_prefill_output_view_without_16_byte_rows(out_dtype):
+    """An output view whose token stride is not a multiple of 16 bytes (d_inner + 1 elements) cannot
+    take the TMA-stored output tiles; the per-lane stores write it, segmented or not, and the
+    element past each row stays untouched."""
+    batch, L, D = 2, 200, 64
+    inp = make_mixer_inputs(batch, L, D, dtype=torch.bfloat16, seed=91)
+    ref = oracle_prefill(inp)
+    g = inp.to("cuda")
+    for seg in (None, 64):
+        buf = torch.full((batch, L, D + 1), 7.0, device="cuda", dtype=out_dtype)
+        out = buf[..., :D]
+        ssm.prefill(g.x, g.z, g.dt, g.B, g.C, g.A, g.D, g.dt_bias, g.conv_w, g.conv_b, out=out, seg_len=seg)
+        torch.cuda.synchronize()
+        extra = half_ulp_bf16(ref["out"]) if out_dtype == torch.bfloat16 else None
+        assert_rms_close(out, ref["out"], 2e-3, f"strided out seg={seg}", extra=extra)
+        assert torch.all(buf[..., D] == 7.0)
