@@ -53,11 +53,7 @@ struct Geo {
                                        ((uint32_t)(kBM >> 4) << 24);
 };
 
-// kPair: the grid is made of 2-CTA clusters along M.  The two CTAs of a cluster compute the
-// tiles (2 mp, n) and (2 mp + 1, n): each loads its own 128 rows of y and one half of the
-// shared 256 rows of W, multicast into both CTAs, so W crosses L2 once per pair.  A stage is
-// refilled only when the MMAs of both CTAs have read it (each commit arrives in both CTAs).
-template <typename Tout, int kBN, bool kPair>
+template <typename Tout, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
 k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
            const OutProjArgs p) {
@@ -78,20 +74,12 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
     const int n_tiles = (int)((p.N + kBN - 1) / kBN);
     const int m_tiles = (int)((p.M + kBM - 1) / kBM);
     const int nk = (int)((p.K + kBK - 1) / kBK);
-    const int rank = kPair ? (int)(blockIdx.x & 1) : 0;
     // this CTA's i-th tile: false when there is none; *m0, *n0 its origin
     auto tile = [&](int i, int* m0, int* n0) -> bool {
-        if (kPair) {
-            const int pt = (int)(blockIdx.x >> 1) + i * (int)(gridDim.x >> 1);
-            if (pt >= n_tiles * ((m_tiles + 1) / 2)) return false;
-            *m0 = (2 * (pt / n_tiles) + rank) * kBM;
-            *n0 = (pt % n_tiles) * kBN;
-        } else {
-            const int t = (int)blockIdx.x + i * (int)gridDim.x;
-            if (t >= n_tiles * m_tiles) return false;
-            *m0 = (t / n_tiles) * kBM;
-            *n0 = (t % n_tiles) * kBN;
-        }
+        const int t = (int)blockIdx.x + i * (int)gridDim.x;
+        if (t >= n_tiles * m_tiles) return false;
+        *m0 = (t / n_tiles) * kBM;
+        *n0 = (t % n_tiles) * kBN;
         return true;
     };
 
@@ -99,7 +87,7 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
         s_err = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kPair ? 2 : 1);
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -116,7 +104,6 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
     }
     tc_fence_before();
     __syncthreads();
-    if (kPair) cluster_sync();                      // the peer's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -134,15 +121,11 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
                 unsigned char* st = smem + s * kStageBytes;
                 mbar_arrive_expect_tx(&full[s], kStageBytes);
                 tma_load_2d(st, &tm_a, &full[s], kb * kBK, m0);
-                if (kPair)
-                    tma_load_2d_mc(st + kABytes + rank * (G::kBBytes / 2), &tm_b, &full[s], kb * kBK,
-                                   n0 + rank * (kBN / 2), (uint16_t)3);
-                else
-                    tma_load_2d(st + kABytes, &tm_b, &full[s], kb * kBK, n0);
+                tma_load_2d(st + kABytes, &tm_b, &full[s], kb * kBK, n0);
             }
         }
-        // tail: every stage's last use has been released by both CTAs' MMAs, so no arrival is
-        // still on its way to this CTA's barriers when it exits
+        // tail: every stage's last use has been released by the MMAs, so no arrival is still on
+        // its way to this CTA's barriers when it exits
         for (int u = it - 1; u >= 0 && u >= it - kStages && !s_err; --u)
             if (!mbar_wait_bounded(&empty[u % kStages], (uint32_t)((u / kStages) & 1))) atomicOr(p.status, 1u);
     } else if (warp == 1 && lane == 0) {
@@ -171,8 +154,7 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
                 for (int kk = 0; kk < kBK / 16; ++kk)      // 16 bf16 = 32 bytes along K per MMA
                     mma_bf16(dt, smem_desc_sw128(a0 + 32 * kk), smem_desc_sw128(b0 + 32 * kk), G::kIdesc,
                              (kb | kk) != 0);
-                if (kPair) mma_commit_mc(&empty[s], (uint16_t)3);   // the stage is free in both CTAs
-                else mma_commit(&empty[s]);
+                mma_commit(&empty[s]);                      // the stage may be refilled
             }
             mma_commit(&acc_full[buf]);                     // the tile is complete in buffer buf
         }
@@ -236,7 +218,6 @@ k_out_proj(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUt
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
-    if (kPair) cluster_sync();                      // neither CTA leaves while its peer may still signal it
 }
 
 // 2-D bf16 map over rows x K (row stride ld elements), box of `rows` x 64, 128-byte swizzle.
@@ -252,60 +233,27 @@ bool make_map_kmajor(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tout, int BN, bool kPair>
+template <typename Tout, int BN>
 int launch_bn(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, int64_t ldw, int dev, int n_sm,
               cudaStream_t stream, const char** why) {
     using G = Geo<BN>;
     CUtensorMap ma, mb;
     if (!make_map_kmajor(&ma, y, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)ldy, kBM) ||
-        !make_map_kmajor(&mb, W, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)ldw, kPair ? BN / 2 : BN)) {
+        !make_map_kmajor(&mb, W, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)ldw, BN)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or layout rejected)";
         return -1;
     }
-    auto kern = k_out_proj<Tout, BN, kPair>;
-    static unsigned long long done = 0;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) != cudaSuccess) {
-            *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
-            return -1;
-        }
-        __atomic_fetch_or(&done, bit, __ATOMIC_ACQ_REL);
-    }
+    auto kern = k_out_proj<Tout, BN>;
+    static ContextMemo attr;
+    if (!opt_in_dynamic_smem(attr, kern, G::kSmemBytes, why)) return -1;
     // persistent: one CTA per SM (the shared memory allows no second one, which also leaves the
-    // SM's TMEM columns to this CTA), looping over the output tiles (or tile pairs)
-    const int64_t m_tiles = (a.M + kBM - 1) / kBM, n_tiles = (a.N + BN - 1) / BN;
+    // SM's TMEM columns to this CTA), looping over the output tiles
+    const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = G::kSmemBytes;
     cfg.stream = stream;
-    if (kPair) {
-        const int64_t pairs = n_tiles * ((m_tiles + 1) / 2);
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        // as many clusters as can be resident at once (a cluster's two CTAs share a GPC),
-        // asked of the runtime once per device and kept
-        static int resident_by_dev[64] = {0};
-        int resident = __atomic_load_n(&resident_by_dev[dev & 63], __ATOMIC_ACQUIRE);
-        if (resident < 1) {
-            cfg.gridDim = dim3((unsigned)(2 * (pairs < n_sm / 2 ? pairs : n_sm / 2)));
-            if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
-                *why = "cudaOccupancyMaxActiveClusters failed";
-                return -1;
-            }
-            __atomic_store_n(&resident_by_dev[dev & 63], resident, __ATOMIC_RELEASE);
-        }
-        const int64_t clusters = pairs < resident ? pairs : resident;
-        cfg.gridDim = dim3((unsigned)(2 * clusters));
-    } else {
-        const int64_t tiles = n_tiles * m_tiles;
-        cfg.gridDim = dim3((unsigned)(tiles < n_sm ? tiles : n_sm));
-    }
+    cfg.gridDim = dim3((unsigned)(tiles < n_sm ? tiles : n_sm));
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -328,12 +276,11 @@ int launch_out_proj(const OutProjArgs& a, const void* y, const void* W, int64_t 
     // 256-column tiles unless that leaves fewer than two tiles per SM; then 128 columns
     const int64_t tiles256 = ((a.N + 255) / 256) * ((a.M + kBM - 1) / kBM);
     const bool narrow = tiles256 < 2 * (int64_t)n_sm;
-    // wide tiles run as 2-CTA clusters sharing the W tile
     if (out_bf16)
-        return narrow ? launch_bn<__nv_bfloat16, 128, false>(a, y, W, ldy, ldw, dev, n_sm, stream, why)
-                      : launch_bn<__nv_bfloat16, 256, true>(a, y, W, ldy, ldw, dev, n_sm, stream, why);
-    return narrow ? launch_bn<float, 128, false>(a, y, W, ldy, ldw, dev, n_sm, stream, why)
-                  : launch_bn<float, 256, true>(a, y, W, ldy, ldw, dev, n_sm, stream, why);
+        return narrow ? launch_bn<__nv_bfloat16, 128>(a, y, W, ldy, ldw, dev, n_sm, stream, why)
+                      : launch_bn<__nv_bfloat16, 256>(a, y, W, ldy, ldw, dev, n_sm, stream, why);
+    return narrow ? launch_bn<float, 128>(a, y, W, ldy, ldw, dev, n_sm, stream, why)
+                  : launch_bn<float, 256>(a, y, W, ldy, ldw, dev, n_sm, stream, why);
 }
 
 }  // namespace ssm
