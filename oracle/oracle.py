@@ -7,6 +7,7 @@ float64 numpy arrays (q8: int32 sums, float32 scales/out, bfloat16 bits).
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import subprocess
 from pathlib import Path
@@ -27,20 +28,30 @@ def lib_path() -> Path:
 
 
 def build(src: Path | None = None, out: Path | None = None, force: bool = False) -> Path:
-    """Compile the oracle with the host C compiler (gcc/cc), OpenMP if available."""
+    """Compile the oracle with the host C compiler (gcc/cc), OpenMP if available.
+
+    A build is reused only when the digest beside it matches the source bytes and compiler,
+    never on file times (a copied tree may carry a library newer than an edited source).
+    """
     src = Path(src) if src else _SRC
     out = Path(out) if out else lib_path()
-    if out.exists() and not force and out.stat().st_mtime >= src.stat().st_mtime:
+    cc = os.environ.get("CC", "gcc")
+    stamp = Path(str(out) + ".sha256")
+    digest = hashlib.sha256(src.read_bytes() + b"\0" + cc.encode()).hexdigest()
+    if (out.exists() and stamp.exists() and not force and
+            stamp.read_text().strip() == digest):
         return out
     out.parent.mkdir(parents=True, exist_ok=True)
-    cc = os.environ.get("CC", "gcc")
+    tmp = f"{out}.{os.getpid()}.tmp"        # concurrent builders (spawned ranks) never share a file
     base = [cc, "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC", str(src),
-            "-o", str(out) + ".tmp", "-lm"]
+            "-o", tmp, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True)
-    os.replace(str(out) + ".tmp", out)
+    os.replace(tmp, out)
+    Path(tmp + ".sha256").write_text(digest + "\n")
+    os.replace(tmp + ".sha256", stamp)
     return out
 
 

@@ -3,9 +3,14 @@
 Each translation unit in ``csrc/`` is compiled by its own nvcc process (in
 parallel), then linked into ``_build/libssm.so``.  ptxas resource usage
 (registers, spills, shared memory) is kept in ``_build/ptxas.log``.
+
+A build is reused only when ``_build/libssm.sha256`` holds the digest of exactly
+the sources, headers, flags and compiler it was made from (file times are not
+trusted: a copied tree keeps a library newer than edited sources).
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -17,6 +22,7 @@ CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 INCLUDE = PKG.parent / "include"
 LIB = BUILD / "libssm.so"
+STAMP = BUILD / "libssm.sha256"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
@@ -39,11 +45,23 @@ def _deps():
         sorted(INCLUDE.glob("*.h"))
 
 
+def source_digest(cc: str | None = None) -> str:
+    """SHA-256 over every source and header (name and bytes), the flags and the compiler path."""
+    h = hashlib.sha256()
+    for p in _deps():
+        h.update(p.name.encode() + b"\0" + p.read_bytes() + b"\0")
+    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update((cc or nvcc()).encode())
+    return h.hexdigest()
+
+
 def up_to_date() -> bool:
-    if not LIB.exists():
+    if not (LIB.exists() and STAMP.exists()):
         return False
-    t = LIB.stat().st_mtime
-    return all(p.stat().st_mtime <= t for p in _deps())
+    try:
+        return STAMP.read_text().strip() == source_digest()
+    except (OSError, RuntimeError):
+        return False
 
 
 def build(force: bool = False, verbose: bool = False) -> Path:
@@ -52,9 +70,12 @@ def build(force: bool = False, verbose: bool = False) -> Path:
         return LIB
     BUILD.mkdir(parents=True, exist_ok=True)
     cc = nvcc()
+    digest = source_digest(cc)
+    objdir = BUILD / f"obj.{os.getpid()}"          # concurrent builders never share an object file
+    objdir.mkdir(exist_ok=True)
 
     def compile_one(src: Path):
-        obj = BUILD / (src.stem + ".o")
+        obj = objdir / (src.stem + ".o")
         cmd = [cc, *NVCC_FLAGS, "-c", str(src), "-o", str(obj)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,12 +85,16 @@ def build(force: bool = False, verbose: bool = False) -> Path:
     with ThreadPoolExecutor(max_workers=max(1, min(len(_sources()), os.cpu_count() or 1))) as ex:
         results = list(ex.map(compile_one, _sources()))
     (BUILD / "ptxas.log").write_text("".join(log for _, log in results))
-    tmp = BUILD / "libssm.so.tmp"
+    tmp = BUILD / f"libssm.so.{os.getpid()}.tmp"       # concurrent builders never share a file
     cmd = [cc, *ARCH, "-shared", "-o", str(tmp), *[str(o) for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    shutil.rmtree(objdir, ignore_errors=True)
+    stamp_tmp = BUILD / f"libssm.sha256.{os.getpid()}.tmp"
+    stamp_tmp.write_text(digest + "\n")
+    os.replace(stamp_tmp, STAMP)
     if verbose:
         print((BUILD / "ptxas.log").read_text())
     return LIB
