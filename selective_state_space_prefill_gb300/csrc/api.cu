@@ -10,10 +10,41 @@
 #include <stdio.h>
 #include <string.h>
 
-#include <atomic>
+#include <cuda.h>
 
 #include "ssm.h"
 #include "kernels.h"
+
+namespace ssm {
+
+uint64_t current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static const GetCurrent get_current = []() -> GetCurrent {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<GetCurrent>(f)
+                   : nullptr;
+    }();
+    static const GetId get_id = []() -> GetId {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<GetId>(f)
+                   : nullptr;
+    }();
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || c == nullptr ||
+        get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+}  // namespace ssm
 
 namespace {
 
@@ -30,26 +61,20 @@ int fail(int code, const char* fmt, ...) {
 // Device status word: SSM_DEV_* bits OR-ed in by kernels.
 __device__ unsigned int g_status_word;
 
-constexpr int kMaxDevices = 64;
-std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+ssm::ContextMemo g_status_memo;
 
-// Device address of the status word for the current device, looked up once per
-// device (with that device current) through cudaGetSymbolAddress.
+// Device address of the status word in the current device's context: a __device__ symbol's
+// name in host code is not a device address, so it is asked of the runtime
+// (cudaGetSymbolAddress) once per device and context.
 unsigned int* status_ptr(int* err) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void* p = nullptr;
+    if (!g_status_memo.get(&p, [](void** out) {
+            return cudaGetSymbolAddress(out, g_status_word) == cudaSuccess && *out != nullptr;
+        })) {
         *err = 1;
         return nullptr;
     }
-    unsigned int* p = g_status_ptr[dev].load(std::memory_order_acquire);
-    if (p) return p;
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess || addr == nullptr) {
-        *err = 1;
-        return nullptr;
-    }
-    g_status_ptr[dev].store(static_cast<unsigned int*>(addr), std::memory_order_release);
-    return static_cast<unsigned int*>(addr);
+    return static_cast<unsigned int*>(p);
 }
 
 }  // namespace
@@ -60,26 +85,20 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCR
 
 namespace {
 
-std::atomic<void*> g_noalloc_scratch_ptr[kMaxDevices];
+ssm::ContextMemo g_noalloc_memo;
 
-// Device address of g_noalloc_scratch on the current device.  In host code the array's name
-// stands for a host-side shadow, not a device address, so the address is asked of the runtime
-// (cudaGetSymbolAddress) once per device, with that device current, and cached.
+// Device address of g_noalloc_scratch in the current device's context.  In host code the
+// array's name stands for a host-side shadow, not a device address, so the address is asked of
+// the runtime (cudaGetSymbolAddress) with that device current, once per device and context.
 void* noalloc_scratch_ptr(int* err) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void* p = nullptr;
+    if (!g_noalloc_memo.get(&p, [](void** out) {
+            return cudaGetSymbolAddress(out, g_noalloc_scratch) == cudaSuccess && *out != nullptr;
+        })) {
         *err = 1;
         return nullptr;
     }
-    void* p = g_noalloc_scratch_ptr[dev].load(std::memory_order_acquire);
-    if (p) return p;
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
-        *err = 1;
-        return nullptr;
-    }
-    g_noalloc_scratch_ptr[dev].store(addr, std::memory_order_release);
-    return addr;
+    return p;
 }
 
 bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -103,7 +122,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
                  void* out, int64_t out_stride_b, int64_t out_stride_t,
                  float* conv_state_out, float* ssm_state_out,
                  int seg_len, void* workspace, size_t workspace_bytes,
-                 void* cuda_stream) {
+                 void* cuda_stream, bool fixed_scratch = false) {
     g_err[0] = 0;
     if (batch < 1 || batch > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: batch %lld not in [1, 65535]", fn, (long long)(batch));
     if (seqlen < 1 || seqlen > (1 << 30)) return fail(SSM_ERR_INVALID_ARG, "%s: seqlen %lld not in [1, 2^30]", fn, (long long)(seqlen));
@@ -137,6 +156,19 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
                     ssm::kPrefillChunk);
     const int64_t n_seg = ((int64_t)seqlen + seg_len - 1) / seg_len;
     if (n_seg > 65535) return fail(SSM_ERR_INVALID_ARG, "%s: %lld segments (at most 65535)", fn, (long long)n_seg);
+    if (n_seg > 1 && fixed_scratch) {
+        // the library's own array stands in for the workspace; every other argument is valid
+        const size_t need = ssm_prefill_workspace_bytes(batch, seqlen, d_inner, seg_len);
+        if (need > (size_t)SSM_NOALLOC_SCRATCH_BYTES)
+            return fail(SSM_ERR_INVALID_ARG,
+                        "%s: these sizes need %zu bytes of scratch and the fixed array holds %zu "
+                        "(use a longer seg_len, or ssm_prefill_segmented with a workspace)",
+                        fn, need, (size_t)SSM_NOALLOC_SCRATCH_BYTES);
+        int err = 0;
+        workspace = noalloc_scratch_ptr(&err);
+        workspace_bytes = (size_t)SSM_NOALLOC_SCRATCH_BYTES;
+        if (err) return fail(SSM_ERR_CUDA, "%s: the scratch array's device address is unavailable", fn);
+    }
     if (n_seg > 1) {
         const size_t need = ssm_prefill_workspace_bytes(batch, seqlen, d_inner, seg_len);
         if (!workspace || workspace_bytes < need)
@@ -230,26 +262,12 @@ int ssm_prefill_segmented_noalloc(int batch, int seqlen, int d_inner, int d_stat
                                   void* out, int64_t out_stride_b, int64_t out_stride_t,
                                   float* conv_state_out, float* ssm_state_out,
                                   int seg_len, void* cuda_stream) {
-    static const char* fn = "ssm_prefill_segmented_noalloc";
-    g_err[0] = 0;
-    const size_t need = ssm_prefill_workspace_bytes(batch, seqlen, d_inner, seg_len);
-    if (need > (size_t)SSM_NOALLOC_SCRATCH_BYTES)
-        return fail(SSM_ERR_INVALID_ARG,
-                    "%s: these sizes need %zu bytes of scratch and the fixed array holds %zu "
-                    "(use a longer seg_len, or ssm_prefill_segmented with a workspace)",
-                    fn, need, (size_t)SSM_NOALLOC_SCRATCH_BYTES);
-    void* ws = nullptr;
-    if (need > 0) {
-        int err = 0;
-        ws = noalloc_scratch_ptr(&err);
-        if (err) return fail(SSM_ERR_CUDA, "%s: the scratch array's device address is unavailable", fn);
-    }
     // Nothing in the array has to start at zero: pass A writes every entry that passes B and C read.
-    return prefill_impl(fn, batch, seqlen, d_inner, d_state, d_conv, in_dtype, out_dtype, x, z, dt,
-                        in_stride_b, in_stride_t, Bmat, Cmat, A, Dskip, dt_bias, conv_w, conv_b, conv_state_in,
-                        ssm_state_in, conv_state_ld, ssm_state_stride_b, out, out_stride_b, out_stride_t,
-                        conv_state_out, ssm_state_out, seg_len, ws, (size_t)SSM_NOALLOC_SCRATCH_BYTES,
-                        cuda_stream);
+    return prefill_impl("ssm_prefill_segmented_noalloc", batch, seqlen, d_inner, d_state, d_conv, in_dtype,
+                        out_dtype, x, z, dt, in_stride_b, in_stride_t, Bmat, Cmat, A, Dskip, dt_bias, conv_w,
+                        conv_b, conv_state_in, ssm_state_in, conv_state_ld, ssm_state_stride_b, out, out_stride_b,
+                        out_stride_t, conv_state_out, ssm_state_out, seg_len, nullptr, 0, cuda_stream,
+                        /*fixed_scratch=*/true);
 }
 
 int ssm_out_proj_partial(int64_t M, int64_t N, int64_t K, const void* y, int64_t ldy, const void* W, int64_t ldw,

@@ -5,7 +5,68 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace ssm {
+
+// ------------------------------------------------------------------ host-side memo
+// Id of the calling thread's current CUDA context (cuCtxGetId), or 0 when no context is
+// current or the driver entry points are missing.
+uint64_t current_context_id();
+
+// Facts that hold for the life of one CUDA context -- a __device__ symbol's address, a
+// kernel's dynamic shared-memory opt-in -- remembered per device together with the id of the
+// context they were taken in.  When the device's current context is a different one (after
+// cudaDeviceReset, or once a new primary context has been made) they are taken again, so a
+// kernel is never handed an address from a context that no longer exists.
+class ContextMemo {
+ public:
+    // *value for the current device and context; compute(&v) runs (and must return true) when
+    // nothing is remembered for that context.
+    template <typename F>
+    bool get(void** value, F&& compute) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return false;
+        uint64_t id = current_context_id();
+        if (id != 0) {
+            std::lock_guard<std::mutex> g(mu_);
+            if (ctx_[dev] == id) {
+                *value = val_[dev];
+                return true;
+            }
+        }
+        void* v = nullptr;
+        if (!compute(&v)) return false;
+        id = current_context_id();     // compute's runtime call has made the context current
+        std::lock_guard<std::mutex> g(mu_);
+        ctx_[dev] = id;                // an id of 0 is never matched: nothing is kept without one
+        val_[dev] = v;
+        *value = v;
+        return true;
+    }
+
+ private:
+    static constexpr int kDevices = 64;
+    std::mutex mu_;
+    uint64_t ctx_[kDevices] = {};
+    void* val_[kDevices] = {};
+};
+
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes) once per device and context.
+template <typename K>
+bool opt_in_dynamic_smem(ContextMemo& memo, K* kern, int bytes, const char** why) {
+    void* v = nullptr;
+    if (!memo.get(&v, [&](void** out) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+                return false;
+            *out = reinterpret_cast<void*>(1);
+            return true;
+        })) {
+        *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+        return false;
+    }
+    return true;
+}
 
 // Kernel-side arguments of the prefill (everything except the TMA maps).
 struct PrefillArgs {

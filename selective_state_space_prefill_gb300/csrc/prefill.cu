@@ -627,24 +627,6 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t
     return r == CUDA_SUCCESS;
 }
 
-// The dynamic shared-memory opt-in is per function and device; *done remembers it per device.
-template <typename F>
-bool opt_in_smem(F* kern, int bytes, unsigned long long* done, const char** why) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        *why = "cudaGetDevice failed";
-        return false;
-    }
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit) return true;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
-        *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
-        return false;
-    }
-    __atomic_fetch_or(done, bit, __ATOMIC_ACQ_REL);
-    return true;
-}
-
 template <int S, int K, typename Tin, typename Tout>
 int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
     using Lay = Layout<S, K, Tin>;
@@ -680,9 +662,9 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
     if (a.n_seg > 1) {
         // pass A (segments 0 .. n_seg-2), then pass B
         using ALay = AggLayout<S, K, Tin>;
-        static unsigned long long agg_attr = 0;
+        static ContextMemo agg_attr;
         auto kagg = k_prefill_agg<S, K, Tin>;
-        if (!opt_in_smem(kagg, ALay::TOTAL, &agg_attr, why)) return -1;
+        if (!opt_in_dynamic_smem(agg_attr, kagg, ALay::TOTAL, why)) return -1;
         kagg<<<dim3(gx, q.batch, a.n_seg - 1), S * 32, ALay::TOTAL, stream>>>(mx, mdt, mB, a);
         const int64_t n = (int64_t)q.batch * a.d_inner * kN;
         k_prefill_carry<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a, q.batch);
@@ -692,9 +674,9 @@ int launch_t(const PrefillLaunch& q, cudaStream_t stream, const char** why) {
             return -1;
         }
     }
-    static unsigned long long attr_row = 0, attr_seg = 0;
+    static ContextMemo attr_row, attr_seg;
     auto kern = a.n_seg > 1 ? k_prefill<S, K, Tin, Tout, true> : k_prefill<S, K, Tin, Tout, false>;
-    if (!opt_in_smem(kern, Lay::TOTAL, a.n_seg > 1 ? &attr_seg : &attr_row, why)) return -1;
+    if (!opt_in_dynamic_smem(a.n_seg > 1 ? attr_seg : attr_row, kern, Lay::TOTAL, why)) return -1;
     kern<<<dim3(gx, q.batch, a.n_seg), S * 32, Lay::TOTAL, stream>>>(mx, mz, mdt, mB, mC, mo, ak);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

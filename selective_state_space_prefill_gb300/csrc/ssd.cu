@@ -912,20 +912,8 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
         return -1;
     }
     auto kern = out_bf16 ? k_ssd_chunk<__nv_bfloat16> : k_ssd_chunk<float>;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        *why = "cudaGetDevice failed";
-        return -1;
-    }
-    static unsigned long long done[2] = {0, 0};
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(__atomic_load_n(&done[out_bf16], __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::ALLOC) != cudaSuccess) {
-            *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
-            return -1;
-        }
-        __atomic_fetch_or(&done[out_bf16], bit, __ATOMIC_ACQ_REL);
-    }
+    static ContextMemo attr[2];
+    if (!opt_in_dynamic_smem(attr[out_bf16 ? 1 : 0], kern, Smem::ALLOC, why)) return -1;
     kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kThAll, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, mo, mds, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -166,6 +166,32 @@ def test_prefill_segmented_single_segment_needs_no_workspace(lib):
     assert _segmented(lib, seg_len=64, ws=FAKE, ws_bytes=3 * 2 * 64 * 128) == CUDA
 
 
+def _noalloc(lib, seg_len=64, **kw):
+    a = dict(batch=2, seqlen=200, d_inner=64, d_state=16, d_conv=4, in_dtype=1, out_dtype=0,
+             x=FAKE, z=FAKE, dt=FAKE, in_stride_b=200 * 64, in_stride_t=64, B=FAKE, C=FAKE, A=FAKE,
+             D=FAKE, dt_bias=FAKE, conv_w=FAKE, conv_b=FAKE, csi=None, ssi=None, ld=64, sb=64 * 16,
+             out=FAKE, ob=200 * 64, ot=64, cso=FAKE, sso=FAKE)
+    a.update(kw)
+    return lib.ssm_prefill_segmented_noalloc(*a.values(), seg_len, None)
+
+
+@pytest.mark.parametrize("kw,code,words", [
+    # a bad seg_len or shape is reported as such, even when the sizes would also overflow the array
+    (dict(seg_len=1, seqlen=1 << 20, d_inner=8192, in_stride_t=8192, in_stride_b=(1 << 20) * 8192,
+          ld=8192, sb=8192 * 16, ot=8192, ob=(1 << 20) * 8192), INVALID, "seg_len 1"),
+    (dict(seg_len=96), INVALID, "seg_len 96"),
+    (dict(d_state=8), UNSUPPORTED, "d_state 8"),
+    (dict(in_stride_t=32), INVALID, "in_stride_t"),
+    # valid arguments whose scratch exceeds the fixed array: the array's limit is named
+    (dict(seqlen=64 * 6, batch=1, d_inner=8192, in_stride_t=8192, in_stride_b=0, ld=8192, sb=8192 * 16,
+          ot=8192, ob=0), INVALID, "fixed array holds"),
+])
+def test_noalloc_validates_arguments_before_the_scratch_limit(lib, kw, code, words):
+    assert _noalloc(lib, **kw) == code
+    msg = lib.ssm_last_error().decode()
+    assert msg.startswith("ssm_prefill_segmented_noalloc") and words in msg, msg
+
+
 def test_suggest_seg_len():
     # 96 channel groups x 1 row on 152 SMs x 3 slots: 4 segments of 512 tokens
     assert binding.suggest_seg_len(1, 2048, 1536, 152) == 512
