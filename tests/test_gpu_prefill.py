@@ -119,9 +119,12 @@ def test_prefill_stream_argument():
 
 
 @pytest.mark.parametrize("seg_len", [None, 128])
-def test_prefill_fp32_seed_sweep(seg_len):
+def test_prefill_fp32_seed_sweep(seg_len, record_property):
     """All-fp32 inputs over 24 seeds (whole rows and 6 segments): outputs reach ~100x their RMS,
-    so the per-element relative bar is what the fp32 path must hold everywhere."""
+    so the per-element relative bar is what the fp32 path must hold everywhere.  The error
+    against 1e-5 x RMS is reported beside it (a plain float32 evaluation of the same formulas
+    reaches 2.6 x that bar on these seeds: tests/test_fp32_tolerance_reading.py)."""
+    worst_rms = 0.0
     for seed in range(20, 44):
         inp = make_mixer_inputs(2, 700, 64, dtype=torch.float32, seed=seed)
         g = inp.to(DEV)
@@ -129,6 +132,12 @@ def test_prefill_fp32_seed_sweep(seg_len):
         ref = oracle_prefill(inp)
         assert_rel_close(out, ref["out"], 1e-5, f"out seed {seed}")
         assert_rel_close(sso, ref["ssm_state"], 1e-5, f"state seed {seed}")
+        for got, r in ((out, ref["out"]), (sso, ref["ssm_state"])):
+            r = np.asarray(r, np.float64)
+            err = np.abs(got.cpu().double().numpy() - r).max()
+            worst_rms = max(worst_rms, float(err / np.sqrt(np.mean(r ** 2))))
+    record_property("max_err_over_rms", worst_rms)
+    print(f"fp32 seed sweep (seg_len {seg_len}): worst max|err| = {worst_rms / 1e-5:.2f} x (1e-5 x RMS)")
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
