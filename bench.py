@@ -1,9 +1,10 @@
 """Benchmark: selective-SSM prefill tokens/s on one GB300 (plus decode steps/s and the q8 reduction).
 
-One step = one ssm_prefill over the Mamba-130M-like layer workload (batch 4, 2048
-tokens, d_inner 1536, d_state 16, conv 4; bf16 x/z/dt/B/C, fp32 A/D/states, fp32
-out), inputs resident in HBM, L2 flushed (a 2x-L2 buffer write) before every timed
-step, each step timed with CUDA events on the launching stream.
+One step = one ssm_prefill over the Zamba-7B-like long-context layer (batch 1, 65536
+tokens, d_inner 7168, d_state 16, conv 4; bf16 x/z/dt/B/C, fp32 A/D/states, fp32
+out), the largest single-GPU workload, inputs resident in HBM, L2 flushed (a 2x-L2
+buffer write) before every timed step, each step timed with CUDA events on the
+launching stream.  ``--workload`` selects another prefill workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -29,14 +30,14 @@ from pathlib import Path
 ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
-# The timed step's workload (--workload); the default is the Mamba-130M-like layer.
+# The timed step's workload (--workload); the default is the Zamba-7B-like long-context layer.
 WORKLOADS = {
     "mamba130m_like_prefill": dict(batch=4, seqlen=2048, d_inner=1536, dtype="bf16"),
     "tiny_mixer_fp32": dict(batch=1, seqlen=256, d_inner=64, dtype="fp32"),
     "falcon_mamba7b_like_slice_prefill": dict(batch=1, seqlen=16384, d_inner=2048, dtype="bf16"),
     "zamba7b_like_long_context_prefill": dict(batch=1, seqlen=65536, d_inner=7168, dtype="bf16"),
 }
-DEFAULT_WORKLOAD = "mamba130m_like_prefill"
+DEFAULT_WORKLOAD = "zamba7b_like_long_context_prefill"
 WORKLOAD = dict(name=DEFAULT_WORKLOAD, d_state=16, d_conv=4, **WORKLOADS[DEFAULT_WORKLOAD])
 
 
@@ -48,6 +49,30 @@ def _set_workload(name):
 def _wdtype(w):
     import torch
     return torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+
+
+def _config(w, world):
+    """The workload as both arms report it."""
+    return {"workload": w["name"], "batch": w["batch"], "seq_len": w["seqlen"], "d_inner": w["d_inner"],
+            "d_state": 16, "d_conv": 4, "inputs": f"{w['dtype']} x/z/dt/B/C, fp32 params and states",
+            "out": "fp32", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed before every timed step (write of a 2x-L2 buffer)"}
+
+
+# Channels of the workload the oracle runs per timed sample (channels are independent, so the
+# whole layer's rate is the sample's rate scaled by d_inner / channels): about 0.5 s per sample
+# on 16 host cores for the long-context layer.
+ORACLE_SAMPLE_CHANNELS = 1024
+
+
+def _oracle_sample(inp, w):
+    """CPU copies of the first ORACLE_SAMPLE_CHANNELS channels of (device) inputs, all tokens."""
+    from selective_state_space_prefill_gb300.inputs import MixerInputs
+    ds = min(w["d_inner"], ORACLE_SAMPLE_CHANNELS)
+    kw = {k: getattr(inp, k)[:, :, :ds].contiguous().cpu() for k in ("x", "z", "dt")}
+    kw.update({k: getattr(inp, k).cpu() for k in ("B", "C")})
+    kw.update({k: getattr(inp, k)[:ds].contiguous().cpu() for k in ("A", "D", "dt_bias", "conv_w", "conv_b")})
+    return MixerInputs(**kw), ds
 METRIC = "prefill tokens/s and decode steps/s per layer; achieved HBM GB/s vs 8 TB/s"
 UNIT = "tokens/s"
 
@@ -92,17 +117,19 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_s: float) -> float
     return world * units_per_rank / slowest_s
 
 
-# DRAM bytes (read + write) of one k_prefill launch on the bench workload, from the ncu capture
-# summarised in profiles/k_prefill_mamba130m_like_b4_l2048_d1536.md, valid only for the prefill
-# source it was taken on (first 16 hex digits of its sha256); any other source reports null.
-PREFILL_NCU_TRAFFIC = {"bytes": 76212480 + 17341440, "prefill_cu_sha256_16": "cb4e88e1f264b8d0"}
+# DRAM bytes (read + write) of one k_prefill launch, from an ncu capture summarised under
+# profiles/, valid only for the workload it was taken on and the prefill source it was taken
+# with (first 16 hex digits of its sha256); anything else reports null.
+PREFILL_NCU_TRAFFIC = {"workload": "mamba130m_like_prefill", "bytes": 76212480 + 17341440,
+                       "prefill_cu_sha256_16": "cb4e88e1f264b8d0"}
 
 
-def _prefill_traffic():
+def _prefill_traffic(workload):
     import hashlib
     src = ROOT / "selective_state_space_prefill_gb300" / "csrc" / "prefill.cu"
     digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    return PREFILL_NCU_TRAFFIC["bytes"] if digest == PREFILL_NCU_TRAFFIC["prefill_cu_sha256_16"] else None
+    ok = workload == PREFILL_NCU_TRAFFIC["workload"] and digest == PREFILL_NCU_TRAFFIC["prefill_cu_sha256_16"]
+    return PREFILL_NCU_TRAFFIC["bytes"] if ok else None
 
 
 # ---------------------------------------------------------------- clocks
@@ -215,29 +242,33 @@ def run_reference(args):
     from selective_state_space_prefill_gb300.inputs import make_mixer_inputs
     import oracle
     w = WORKLOAD
-    inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=_wdtype(w), seed=0)
+    # the same seeded draws as the timed arm (its generator runs on the device when there is one)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_mixer_inputs(w["batch"], w["seqlen"], w["d_inner"], dtype=_wdtype(w), seed=0, device=gen_dev)
+    smp, ds = _oracle_sample(inp, w)
+    del inp
     threads = _host_cores()
     oracle.build()
     for _ in range(args.warmup):
-        _cpu_oracle_run(inp, 0.0, threads)
+        _cpu_oracle_run(smp, 0.0, threads)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _cpu_oracle_run(inp, 0.0, threads)
+        _cpu_oracle_run(smp, 0.0, threads)
         times.append(time.perf_counter() - t0)
     total = sum(times)
-    tokens = w["batch"] * w["seqlen"] * args.steps
+    tokens = w["batch"] * w["seqlen"] * args.steps * ds / w["d_inner"]
     value = tokens / total
+    sample = (f"{ds} of {w['d_inner']} channels x {w['batch']} x {w['seqlen']} tokens per step (channels are "
+              f"independent; tokens/s scaled by {w['d_inner']}/{ds})" if ds < w["d_inner"] else
+              f"the whole workload (all {w['d_inner']} channels x {w['batch']} x {w['seqlen']} tokens) per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) tokens, Mamba-style parameters)",
-        "config": {"workload": w["name"], "batch": w["batch"], "seq_len": w["seqlen"], "d_inner": w["d_inner"],
-                   "d_state": 16, "d_conv": 4, "inputs": w["dtype"]},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"the whole workload (all {w['d_inner']} channels x {w['batch']} x "
-                                   f"{w['seqlen']} tokens) per step"},
+        "data": "synthetic (seeded N(0,1) tokens; A=-(n+1), D=1, log-uniform dt_bias, U(-.5,.5) conv)",
+        "config": _config(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -319,7 +350,7 @@ def run_ours(args):
     fp32_peak = n_sm * 128 * sm_max * 1e6 / 1e12           # TFLOP/s-equivalent: FP32-pipe lane-ops/s
     fp32_ach = prefill_fp32_ops(B, L, D) / avg_s / 1e12
     roofline = {"bound": "alu", "achieved": fp32_ach, "peak": fp32_peak, "unit": "T fp32-ops/s",
-                "frac": fp32_ach / fp32_peak, "traffic": _prefill_traffic() if w["name"] == DEFAULT_WORKLOAD else None,
+                "frac": fp32_ach / fp32_peak, "traffic": _prefill_traffic(w["name"]),
                 "traffic_unit": "DRAM bytes per launch (ncu)",
                 "kernel": "k_prefill", "peak_source": f"{n_sm} SMs x 128 FP32 lanes x {sm_max:.0f} MHz",
                 "hbm": {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -346,14 +377,17 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
         oracle.build()
-        cpu_inp = inp.to("cpu")
+        smp, ds = _oracle_sample(inp, w)
         threads = _host_cores()
-        reps, el = _cpu_oracle_run(cpu_inp, args.cpu_seconds, threads)
-        cpu = {"value": reps * B * L / el, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"the whole workload (all {D} channels x {B} x {L} tokens), {reps} run(s) in {el:.1f} s"}
+        reps, el = _cpu_oracle_run(smp, args.cpu_seconds, threads)
+        cpu = {"value": reps * B * L * ds / D / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": (f"{ds} of {D} channels x {B} x {L} tokens (tokens/s scaled by {D}/{ds}: channels are "
+                          f"independent), {reps} run(s) in {el:.1f} s" if ds < D else
+                          f"the whole workload (all {D} channels x {B} x {L} tokens), {reps} run(s) in {el:.1f} s")}
+        cpu_inp = smp
         # one host thread on a channel sample (channels are independent, so the rate scales)
         import oracle as _orc
-        n1 = min(96, D)
+        n1 = min(16 if L > 8192 else 96, ds)
         t1 = time.perf_counter()
         _orc.prefill(cpu_inp.x, cpu_inp.z, cpu_inp.dt, cpu_inp.B, cpu_inp.C, cpu_inp.A, cpu_inp.D, cpu_inp.dt_bias,
                      cpu_inp.conv_w, cpu_inp.conv_b, channels=list(range(n1)), n_threads=1)
@@ -364,14 +398,14 @@ def run_ours(args):
         # so a layer's rate is the sample's rate scaled by the channel ratio)
         from selective_state_space_prefill_gb300.inputs import make_decode_inputs, make_mixer_params, make_states
         other = {}
-        for name, (Lo, Do, ds) in {"falcon_mamba7b_like_slice_L16384_d2048": (16384, 2048, 512),
-                                   "zamba7b_like_L65536_d7168": (65536, 7168, 256)}.items():
-            smp = make_mixer_inputs(1, Lo, ds, dtype=torch.bfloat16, seed=0)
+        for name, (Bo, Lo, Do, ds) in {"falcon_mamba7b_like_slice_L16384_d2048": (1, 16384, 2048, 512),
+                                       "mamba130m_like_b4_L2048_d1536": (4, 2048, 1536, 1536)}.items():
+            smp = make_mixer_inputs(Bo, Lo, ds, dtype=torch.bfloat16, seed=0)
             t2 = time.perf_counter()
             _orc.prefill(smp.x, smp.z, smp.dt, smp.B, smp.C, smp.A, smp.D, smp.dt_bias, smp.conv_w, smp.conv_b,
                          n_threads=threads)
             t2 = time.perf_counter() - t2
-            other[name] = {"tokens_per_s": Lo * ds / Do / t2, "sample": f"{ds} of {Do} channels, {t2:.2f} s"}
+            other[name] = {"tokens_per_s": Bo * Lo * ds / Do / t2, "sample": f"{ds} of {Do} channels, {t2:.2f} s"}
         Bd, Dd = 256, 8192
         tok = make_decode_inputs(Bd, Dd, seed=Bd)
         par = make_mixer_params(Dd, seed=1)
@@ -389,10 +423,7 @@ def run_ours(args):
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded N(0,1) tokens; A=-(n+1), D=1, log-uniform dt_bias, U(-.5,.5) conv)",
-            "config": {"workload": w["name"], "batch": B, "seq_len": L, "d_inner": D, "d_state": 16, "d_conv": 4,
-                       "inputs": f"{w['dtype']} x/z/dt/B/C, fp32 params and states", "out": "fp32",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "flushed before every timed step (write of a 2x-L2 buffer)"},
+            "config": _config(w, world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": {k: cs[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
             "wall_s_timed_region": t_wall, "device_status": status,
@@ -465,7 +496,8 @@ def bench_e2e(ssm, inp, dev, steps, world, B, L, D):
 
 
 def bench_prefill_other(ssm, dev, stream, hbm_peak, flush):
-    """Prefill tokens/s on the long-context and channel-slice workloads and on a batch-1
+    """Prefill tokens/s on the other prefill workloads: the batch-4 Mamba-130M-like layer, the
+    unsplit 8192-channel Falcon-Mamba-like layer and one 2048-channel slice of it, and a batch-1
     Mamba-130M-like layer (5 timed launches each, L2 flushed before each).  Batch-1 rows
     are also timed with the sequence cut into parallel segments (ssm_prefill_segmented,
     seg_len from binding.suggest_seg_len) when they leave SMs idle."""
@@ -473,7 +505,8 @@ def bench_prefill_other(ssm, dev, stream, hbm_peak, flush):
     from selective_state_space_prefill_gb300.inputs import make_mixer_inputs
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {}
-    for name, (Bt, L, D) in {"zamba7b_like_L65536_d7168": (1, 65536, 7168),
+    for name, (Bt, L, D) in {"mamba130m_like_b4_L2048_d1536": (4, 2048, 1536),
+                             "falcon_mamba7b_like_unsplit_L16384_d8192": (1, 16384, 8192),
                              "falcon_mamba7b_like_slice_L16384_d2048": (1, 16384, 2048),
                              "mamba130m_like_batch1_L2048_d1536": (1, 2048, 1536)}.items():
         inp = make_mixer_inputs(Bt, L, D, dtype=torch.bfloat16, seed=0, device=dev)
@@ -919,7 +952,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD,
-                    help="the prefill workload of the timed step (default: the Mamba-130M-like layer)")
+                    help="the prefill workload of the timed step (default: the Zamba-7B-like long-context layer)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
