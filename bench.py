@@ -120,8 +120,8 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_s: float) -> float
 # DRAM bytes (read + write) of one k_prefill launch, from an ncu capture summarised under
 # profiles/, valid only for the workload it was taken on and the prefill source it was taken
 # with (first 16 hex digits of its sha256); anything else reports null.
-PREFILL_NCU_TRAFFIC = {"workload": "mamba130m_like_prefill", "bytes": 76212480 + 17341440,
-                       "prefill_cu_sha256_16": "cb4e88e1f264b8d0"}
+PREFILL_NCU_TRAFFIC = {"workload": "zamba7b_like_long_context_prefill", "bytes": 3.02e9 + 1.85e9,
+                       "prefill_cu_sha256_16": "b8bfb22367bf380d"}
 
 
 def _prefill_traffic(workload):
@@ -367,6 +367,7 @@ def run_ours(args):
     if not args.no_extras:
         extras["decode"] = bench_decode(ssm, dev, stream, hbm_peak)
         extras["q8"] = bench_q8(ssm, dev, stream, hbm_peak, flush)
+        extras["q8_split"] = bench_q8_split(ssm, dev, stream, hbm_peak, flush)
         extras["prefill_other_workloads"] = bench_prefill_other(ssm, dev, stream, hbm_peak, flush)
         extras["decode_block"] = bench_decode_block(ssm, dev, stream, hbm_peak, flush)
         extras["out_proj"] = bench_out_proj(ssm, dev, stream, flush, _tc_peak())
@@ -876,6 +877,53 @@ def bench_q8(ssm, dev, stream, hbm_peak, flush, P=4, graph_calls=64):
                    "batch <= 256: CUDA graph of back-to-back calls with L2-resident operands, so GB_s there "
                    "is not an HBM figure; batch 4096 and 16384 (2^26 elements) are extended sizes showing the "
                    "bandwidth regime")
+    return res
+
+
+def bench_q8_split(ssm, dev, stream, hbm_peak, flush, P=4, batch=16384):
+    """The rank-local halves of the 8-bit all-reduce on one rank's partial of the extended
+    reduction size (bf16 [16384, 1, 4096], 2^26 elements): block maxima, shared-scale codes,
+    and the sum of P = 4 ranks' codes with bf16 output and int32 sums.  Each kernel is timed
+    alone (10 launches, L2 flushed before each) against the bytes it must move."""
+    import torch
+    from selective_state_space_prefill_gb300.inputs import make_partials
+    n = batch * 4096
+    nblk = n // 128
+    parts = [p.to(dev) for p in make_partials(P, (batch, 1, 4096), dtype=torch.bfloat16, seed=batch)]
+    amax = torch.empty(nblk, device=dev)
+    codes = [torch.empty(batch, 1, 4096, device=dev, dtype=torch.int8) for _ in range(P)]
+    scales = torch.empty(nblk, device=dev)
+    out = torch.empty(batch, 1, 4096, device=dev, dtype=torch.bfloat16)
+    sums = torch.empty(n, device=dev, dtype=torch.int32)
+    ssm.q8_block_absmax(parts[0], out=amax, stream=stream)
+    for p, c in zip(parts, codes):
+        ssm.q8_quantize_shared(p, amax, codes=c, scales=scales, stream=stream)
+    steps = {
+        "block_absmax": (lambda: ssm.q8_block_absmax(parts[0], out=amax, stream=stream), 2 * n + 4 * nblk),
+        "quantize_shared": (lambda: ssm.q8_quantize_shared(parts[0], amax, codes=codes[0], scales=scales,
+                                                           stream=stream), 2 * n + n + 8 * nblk),
+        "sum_dequant_P4": (lambda: ssm.q8_sum_dequant(codes, scales, out=out, sums=sums, stream=stream),
+                           P * n + 2 * n + 4 * n + 4 * nblk),
+    }
+    res = {}
+    for name, (f, nbytes) in steps.items():
+        for _ in range(3):
+            f()
+        times = []
+        for k in range(10):
+            flush.fill_(float(k))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        t = statistics.median(a.elapsed_time(b) for a, b in times) / 1e3
+        gbs = nbytes / t / 1e9
+        res[name] = {"us": 1e6 * t, "GB_s": gbs, "frac_hbm": gbs / hbm_peak}
+    res["note"] = ("one rank's share of the quantized all-reduce across GPUs (q8_block_absmax, "
+                   "q8_quantize_shared, q8_sum_dequant); the MAX all-reduce of the maxima and the "
+                   "all-gather of the codes are the collectives between them")
     return res
 
 

@@ -322,10 +322,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int t_own = tbase + KH * g;
 #pragma unroll
         for (int k = 0; k < KH; ++k) {
-            const float o0 = __shfl_xor_sync(0xffffffffu, ylane[k], 16);
-            const float o1 = __shfl_xor_sync(0xffffffffu, ylane[KH + k], 16);
+            // each half sends the other the partial readout of the other's token: one shuffle
             const float mine = g ? ylane[KH + k] : ylane[k];
-            const float other = g ? o1 : o0;
+            const float other = __shfl_xor_sync(0xffffffffu, g ? ylane[k] : ylane[KH + k], 16);
             const int t = t_own + k;
             if (dvalid && t < L) {
                 const float yv = (mine + other) + ud[k];
