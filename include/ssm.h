@@ -317,6 +317,41 @@ int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype,
                        float* scales_out, void* cuda_stream);
 
 /*
+ * The rank-local halves of the 8-bit all-reduce (Methodology 4) for partials that live on
+ * different GPUs.  q8_reduce_partials needs all P partials in one memory; a tensor-parallel
+ * rank holds only its own.  The same arithmetic then runs as:
+ *   1. q8_block_absmax on the rank's partial (ssm_out_proj_partial emits the same maxima);
+ *   2. a MAX all-reduce of those maxima across the ranks (the caller's collective);
+ *   3. q8_quantize_shared: the rank's int8 codes with the shared per-block scale;
+ *   4. an all-gather of the ranks' codes (the caller's collective; 1 byte per element);
+ *   5. q8_sum_dequant over the P code buffers.
+ * Steps 5 o 3 with the maximum of step 1 over the ranks give q8_reduce_partials' sums,
+ * scales and outputs bit for bit, because every step is the same correctly rounded fp32
+ * operation.  Shapes as in q8_reduce_partials; block must be 128; every device pointer
+ * 16-byte aligned; n >= 1.  Non-finite values: a NaN is ignored by the block maximum and
+ * gets code 0; a block whose maximum is +inf gets codes 0, scale +inf and NaN outputs.
+ */
+
+/* block_amax[j] = max |x_i| over block j of 128 consecutive elements of x ([n] in_dtype);
+ * block_amax holds ceil(n / 128) float32. */
+int q8_block_absmax(const void* x, ssm_dtype_t in_dtype, int64_t n, int block, float* block_amax,
+                    void* cuda_stream);
+
+/* With the shared maxima amax[j] (the maximum of every rank's block_amax): codes[i] =
+ * round_half_even(x_i * (127 / amax[j])) clamped to [-127, 127] (0 when amax[j] is 0);
+ * scales_out (NULL or [ceil(n / 128)] float32) = amax[j] / 127 (IEEE fp32 division).
+ * codes: [n] int8, written. */
+int q8_quantize_shared(const void* x, ssm_dtype_t in_dtype, int64_t n, int block, const float* block_amax,
+                       int8_t* codes, float* scales_out, void* cuda_stream);
+
+/* S[i] = sum over the P code buffers of codes_p[i] (int32); out[i] = float(S[i]) * scales[j]
+ * (fp32, then round to nearest even for bf16 out).  codes: HOST array of P (1..8) device
+ * pointers to [n] int8; scales: [ceil(n / 128)] float32 from q8_quantize_shared (the same on
+ * every rank); sums_out: NULL or [n] int32. */
+int q8_sum_dequant(int P, const int8_t* const* codes, const float* scales, int64_t n, int block,
+                   void* out, ssm_dtype_t out_dtype, int32_t* sums_out, void* cuda_stream);
+
+/*
  * The SSD (Mamba-2-style) variant of the mixer.  The pages name the model families the
  * mixer serves (Overview: Mamba, Falcon-Mamba, Zamba) but print no equations for this
  * form; it follows the published Mamba-2 layer (Dao and Gu, "Transformers are SSMs",

@@ -16,7 +16,10 @@ from .oracle import (  # noqa: F401
     lib_path,
     out_proj,
     prefill,
+    q8_block_absmax,
+    q8_quantize_shared,
     q8_reduce,
+    q8_sum_dequant,
     scan_chunked,
     scan_sequential,
     ssd_prefill,

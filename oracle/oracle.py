@@ -67,6 +67,12 @@ def _bind(lib):
     lib.oracle_scan_chunked.restype = None
     lib.oracle_q8_reduce.argtypes = [I, P, I, L, I, P, P, P, P]
     lib.oracle_q8_reduce.restype = I
+    lib.oracle_q8_block_absmax.argtypes = [P, I, L, I, P]
+    lib.oracle_q8_block_absmax.restype = I
+    lib.oracle_q8_quantize_shared.argtypes = [P, I, L, I, P, P, P]
+    lib.oracle_q8_quantize_shared.restype = I
+    lib.oracle_q8_sum_dequant.argtypes = [I, P, P, L, I, P, P, P]
+    lib.oracle_q8_sum_dequant.restype = I
     lib.oracle_out_proj.argtypes = [L, L, L, I, P, P, P, P, P, I]
     lib.oracle_out_proj.restype = I
     lib.oracle_ssd_prefill.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I,
@@ -243,6 +249,49 @@ def q8_reduce(partials, block=128, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_q8_reduce rejected the sizes (rc={rc})")
     return dict(sums=sums, scales=scales, out_f32=out_f32, out_bf16=out_bf16)
+
+
+def q8_block_absmax(x, block=128, lib=None):
+    """float32 [nblk] block maxima of |x| (x flattened)."""
+    lib = lib or load()
+    r, code = _raw(x)
+    a = np.ascontiguousarray(r.reshape(-1))
+    n = a.size
+    amax = np.empty((n + block - 1) // block, np.float32)
+    if lib.oracle_q8_block_absmax(a.ctypes.data, code, n, block, _p(amax)) != 0:
+        raise ValueError("oracle_q8_block_absmax rejected the sizes")
+    return amax
+
+
+def q8_quantize_shared(x, amax, block=128, lib=None):
+    """Returns dict(codes int8 [n], scales float32 [nblk]) for the shared maxima `amax`."""
+    lib = lib or load()
+    r, code = _raw(x)
+    a = np.ascontiguousarray(r.reshape(-1))
+    n = a.size
+    am = np.ascontiguousarray(np.asarray(amax, np.float32).reshape(-1))
+    codes = np.empty(n, np.int8)
+    scales = np.empty((n + block - 1) // block, np.float32)
+    if lib.oracle_q8_quantize_shared(a.ctypes.data, code, n, block, _p(am), _p(codes), _p(scales)) != 0:
+        raise ValueError("oracle_q8_quantize_shared rejected the sizes")
+    return dict(codes=codes, scales=scales)
+
+
+def q8_sum_dequant(codes, scales, block=128, lib=None):
+    """codes: P int8 arrays [n]; returns dict(sums int32, out_f32 float32, out_bf16 uint16 bits)."""
+    lib = lib or load()
+    cs = [np.ascontiguousarray(np.asarray(c, np.int8).reshape(-1)) for c in codes]
+    n = cs[0].size
+    P = len(cs)
+    ptrs = (ctypes.c_void_p * P)(*[c.ctypes.data for c in cs])
+    sc = np.ascontiguousarray(np.asarray(scales, np.float32).reshape(-1))
+    sums = np.empty(n, np.int32)
+    out_f32 = np.empty(n, np.float32)
+    out_bf16 = np.empty(n, np.uint16)
+    if lib.oracle_q8_sum_dequant(P, ctypes.cast(ptrs, ctypes.c_void_p), _p(sc), n, block, _p(sums), _p(out_f32),
+                                 _p(out_bf16)) != 0:
+        raise ValueError("oracle_q8_sum_dequant rejected the sizes")
+    return dict(sums=sums, out_f32=out_f32, out_bf16=out_bf16)
 
 
 def out_proj(y, W, n_threads=None, lib=None):

@@ -302,6 +302,71 @@ int oracle_q8_reduce(int P, const void* const* partials, int in_dtype, int64_t n
 }
 
 /*
+ * The rank-local halves of the quantized all-reduce (Methodology 4) when every rank holds
+ * only its own partial, in fp32 like oracle_q8_reduce (the last block may be shorter):
+ *   oracle_q8_block_absmax:    amax[j] = max_{i in block j} |x_i|   (a NaN is ignored)
+ *   oracle_q8_quantize_shared: given the maxima shared by all ranks (the maximum over the
+ *       ranks of their amax), inv = 127/amax_j and scale_j = amax_j/127 (both 0 when
+ *       amax_j is 0 or not a number), q_i = clamp(rint(x_i * inv), -127, 127), a NaN
+ *       product giving 0
+ *   oracle_q8_sum_dequant:     S_i = sum_p q_p,i (int32), out_i = (float)S_i * scale_j
+ * Combining the ranks' maxima by max and composing the three gives the steps of
+ * oracle_q8_reduce.
+ */
+int oracle_q8_block_absmax(const void* x, int in_dtype, int64_t n, int block, float* amax)
+{
+    if (n < 0 || block < 1) return -1;
+    for (int64_t j0 = 0; j0 < n; j0 += block) {
+        const int64_t j1 = j0 + block < n ? j0 + block : n;
+        float m = 0.0f;
+        for (int64_t i = j0; i < j1; ++i) {
+            const float v = fabsf(widen_f32(x, in_dtype, i));
+            if (v > m) m = v;
+        }
+        amax[j0 / block] = m;
+    }
+    return 0;
+}
+
+int oracle_q8_quantize_shared(const void* x, int in_dtype, int64_t n, int block, const float* amax,
+                              int8_t* codes, float* scales)
+{
+    if (n < 0 || block < 1) return -1;
+    for (int64_t j0 = 0; j0 < n; j0 += block) {
+        const int64_t j1 = j0 + block < n ? j0 + block : n;
+        const float a = amax[j0 / block];
+        float inv = 0.0f, scale = 0.0f;
+        if (a > 0.0f) {
+            inv = 127.0f / a;
+            scale = a / 127.0f;
+        }
+        if (scales) scales[j0 / block] = scale;
+        for (int64_t i = j0; i < j1; ++i) {
+            float r = rintf(widen_f32(x, in_dtype, i) * inv);
+            if (r != r) r = 0.0f;
+            r = r > 127.0f ? 127.0f : (r < -127.0f ? -127.0f : r);
+            codes[i] = (int8_t)r;
+        }
+    }
+    return 0;
+}
+
+int oracle_q8_sum_dequant(int P, const int8_t* const* codes, const float* scales, int64_t n, int block,
+                          int32_t* sums, float* out_f32, uint16_t* out_bf16)
+{
+    if (P < 1 || n < 0 || block < 1) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        int32_t s = 0;
+        for (int p = 0; p < P; ++p) s += codes[p][i];
+        const float o = (float)s * scales[i / block];
+        if (sums) sums[i] = s;
+        if (out_f32) out_f32[i] = o;
+        if (out_bf16) out_bf16[i] = f32_to_bf16_rne(o);
+    }
+    return 0;
+}
+
+/*
  * oracle_out_proj -- one tensor-parallel rank's partial of the mixer's output
  * projection, the operand of the quantized all-reduce ("Scaling State-Space
  * Models on Multiple GPUs with Tensor Parallelism", Methodology 1: the layer is

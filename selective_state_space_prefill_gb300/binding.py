@@ -22,7 +22,8 @@ DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 1, 2
 
 EXPORTS = ("ssm_abi_version", "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_segmented",
            "ssm_prefill_segmented_noalloc", "ssm_decode_step", "ssm_decode_tokens", "ssm_out_proj_partial",
-           "q8_reduce_partials", "ssd_prefill_workspace_bytes", "ssd_prefill", "ssd_decode_step",
+           "q8_reduce_partials", "q8_block_absmax", "q8_quantize_shared", "q8_sum_dequant",
+           "ssd_prefill_workspace_bytes", "ssd_prefill", "ssd_decode_step",
            "ssm_selftest_expire_wait", "ssm_device_status", "ssm_last_error")
 NOALLOC_SCRATCH_BYTES = 4 << 20     # SSM_NOALLOC_SCRATCH_BYTES
 
@@ -70,6 +71,12 @@ def load(path: Path | str | None = None):
     lib.ssm_out_proj_partial.restype = I
     lib.q8_reduce_partials.argtypes = [I, P, I, L, I, P, I, P, P, P]
     lib.q8_reduce_partials.restype = I
+    lib.q8_block_absmax.argtypes = [P, I, L, I, P, P]
+    lib.q8_block_absmax.restype = I
+    lib.q8_quantize_shared.argtypes = [P, I, L, I, P, P, P, P]
+    lib.q8_quantize_shared.restype = I
+    lib.q8_sum_dequant.argtypes = [I, P, P, L, I, P, I, P, P]
+    lib.q8_sum_dequant.restype = I
     lib.ssd_prefill_workspace_bytes.argtypes = [I, I, I, I]
     lib.ssd_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_prefill.argtypes = [I, I, I, I, I, I, I, I, I, P, L, L, P, L, L, P, L, L, P, P, P, P, P, P, P,
@@ -331,6 +338,70 @@ def q8_reduce(partials, block=128, out=None, out_dtype=None, sums=None, scales=N
                                 _ptr(out), _dtype_code(out.dtype), _ptr(sums), _ptr(scales), _stream(stream))
     _check(lib, "q8_reduce_partials", rc)
     return out, sums, scales
+
+
+def q8_block_absmax(x, block=128, out=None, stream=None):
+    """q8_block_absmax: per-128-block maxima of |x| (x flattened, contiguous) -> float32 [nblk]."""
+    lib = load()
+    _need_cuda(x, out)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    n = x.numel()
+    if out is None:
+        out = torch.empty((n + block - 1) // block, device=x.device, dtype=torch.float32)
+    rc = lib.q8_block_absmax(_ptr(x), _dtype_code(x.dtype), n, block, _ptr(out), _stream(stream))
+    _check(lib, "q8_block_absmax", rc)
+    return out
+
+
+def q8_quantize_shared(x, block_amax, block=128, codes=None, scales=None, stream=None):
+    """q8_quantize_shared: int8 codes of x with the shared per-block maxima.
+
+    Returns (codes int8 shaped like x, scales float32 [nblk]); pass scales=False to skip them.
+    """
+    lib = load()
+    _need_cuda(x, block_amax, codes)
+    if not x.is_contiguous() or not block_amax.is_contiguous() or block_amax.dtype != torch.float32:
+        raise ValueError("x and block_amax (float32) must be contiguous")
+    n = x.numel()
+    nblk = (n + block - 1) // block
+    if block_amax.numel() != nblk:
+        raise ValueError(f"block_amax holds {block_amax.numel()} maxima, {nblk} needed")
+    if codes is None:
+        codes = torch.empty(x.shape, device=x.device, dtype=torch.int8)
+    if scales is None:
+        scales = torch.empty(nblk, device=x.device, dtype=torch.float32)
+    scales = scales if scales is not False else None
+    rc = lib.q8_quantize_shared(_ptr(x), _dtype_code(x.dtype), n, block, _ptr(block_amax), _ptr(codes),
+                                _ptr(scales), _stream(stream))
+    _check(lib, "q8_quantize_shared", rc)
+    return codes, scales
+
+
+def q8_sum_dequant(codes, scales, block=128, out=None, out_dtype=torch.float32, sums=None, stream=None):
+    """q8_sum_dequant over P equal-shaped int8 code tensors with their shared scales.
+
+    Returns (out, sums int32 [n]); pass sums=False to skip them.
+    """
+    lib = load()
+    _need_cuda(*codes, scales, out)
+    P = len(codes)
+    shape = codes[0].shape
+    for c in codes:
+        if c.shape != shape or c.dtype != torch.int8 or not c.is_contiguous():
+            raise ValueError("codes must be contiguous int8 tensors of one shape")
+    n = codes[0].numel()
+    dev = codes[0].device
+    if out is None:
+        out = torch.empty(shape, device=dev, dtype=out_dtype)
+    if sums is None:
+        sums = torch.empty(n, device=dev, dtype=torch.int32)
+    sums = sums if sums is not False else None
+    ptrs = (ctypes.c_void_p * P)(*[c.data_ptr() for c in codes])
+    rc = lib.q8_sum_dequant(P, ctypes.cast(ptrs, ctypes.c_void_p), _ptr(scales), n, block, _ptr(out),
+                            _dtype_code(out.dtype), _ptr(sums), _stream(stream))
+    _check(lib, "q8_sum_dequant", rc)
+    return out, sums
 
 
 def device_status(clear: bool = True) -> int:

@@ -224,7 +224,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
 
 extern "C" {
 
-int ssm_abi_version(void) { return 106; }
+int ssm_abi_version(void) { return 107; }
 
 const char* ssm_last_error(void) { return g_err; }
 
@@ -643,6 +643,60 @@ int q8_reduce_partials(int P, const void* const* partials, ssm_dtype_t in_dtype,
     const char* why = "";
     if (ssm::launch_q8(a, in_dtype == SSM_BF16, out_dtype == SSM_BF16, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
         return fail(SSM_ERR_CUDA, "q8_reduce_partials: %s", why);
+    return SSM_OK;
+}
+
+int q8_block_absmax(const void* x, ssm_dtype_t in_dtype, int64_t n, int block, float* block_amax,
+                    void* cuda_stream) {
+    static const char* fn = "q8_block_absmax";
+    g_err[0] = 0;
+    if (!x || !block_amax) return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (n < 1) return fail(SSM_ERR_INVALID_ARG, "%s: n %lld < 1", fn, (long long)n);
+    if (block != 128) return fail(SSM_ERR_UNSUPPORTED, "%s: block %d unsupported (128 only)", fn, block);
+    if (!dtype_ok(in_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (!aligned(x, 16) || !aligned(block_amax, 4)) return fail(SSM_ERR_MISALIGNED, "%s: x must be 16-byte aligned", fn);
+    const char* why = "";
+    if (ssm::launch_q8_absmax(x, in_dtype == SSM_BF16, n, block_amax, static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
+    return SSM_OK;
+}
+
+int q8_quantize_shared(const void* x, ssm_dtype_t in_dtype, int64_t n, int block, const float* block_amax,
+                       int8_t* codes, float* scales_out, void* cuda_stream) {
+    static const char* fn = "q8_quantize_shared";
+    g_err[0] = 0;
+    if (!x || !block_amax || !codes) return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (n < 1) return fail(SSM_ERR_INVALID_ARG, "%s: n %lld < 1", fn, (long long)n);
+    if (block != 128) return fail(SSM_ERR_UNSUPPORTED, "%s: block %d unsupported (128 only)", fn, block);
+    if (!dtype_ok(in_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(block_amax, 4) || (scales_out && !aligned(scales_out, 4)))
+        return fail(SSM_ERR_MISALIGNED, "%s: x and codes must be 16-byte aligned", fn);
+    const char* why = "";
+    if (ssm::launch_q8_quantize(x, in_dtype == SSM_BF16, n, block_amax, codes, scales_out,
+                                static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
+    return SSM_OK;
+}
+
+int q8_sum_dequant(int P, const int8_t* const* codes, const float* scales, int64_t n, int block,
+                   void* out, ssm_dtype_t out_dtype, int32_t* sums_out, void* cuda_stream) {
+    static const char* fn = "q8_sum_dequant";
+    g_err[0] = 0;
+    if (P < 1 || P > ssm::kMaxPartials) return fail(SSM_ERR_UNSUPPORTED, "%s: P %d not in [1, 8]", fn, P);
+    if (!codes || !scales || !out) return fail(SSM_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (n < 1) return fail(SSM_ERR_INVALID_ARG, "%s: n %lld < 1", fn, (long long)n);
+    if (block != 128) return fail(SSM_ERR_UNSUPPORTED, "%s: block %d unsupported (128 only)", fn, block);
+    if (!dtype_ok(out_dtype)) return fail(SSM_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    for (int p = 0; p < P; ++p) {
+        if (!codes[p]) return fail(SSM_ERR_INVALID_ARG, "%s: codes[%d] is NULL", fn, p);
+        if (!aligned(codes[p], 16)) return fail(SSM_ERR_MISALIGNED, "%s: codes[%d] not 16-byte aligned", fn, p);
+    }
+    if (!aligned(out, 16) || !aligned(scales, 4) || (sums_out && !aligned(sums_out, 16)))
+        return fail(SSM_ERR_MISALIGNED, "%s: out and sums must be 16-byte aligned", fn);
+    const char* why = "";
+    if (ssm::launch_q8_sum(P, codes, scales, n, out, out_dtype == SSM_BF16, sums_out,
+                           static_cast<cudaStream_t>(cuda_stream), &why) != 0)
+        return fail(SSM_ERR_CUDA, "%s: %s", fn, why);
     return SSM_OK;
 }
 

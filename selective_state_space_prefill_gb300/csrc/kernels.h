@@ -187,6 +187,13 @@ int launch_ssd_decode(const SsdDecodeArgs& a, bool in_bf16, bool out_bf16, cudaS
 int launch_prefill(const PrefillLaunch& q, cudaStream_t stream, const char** why);
 int launch_decode(const DecodeArgs& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
 int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why);
+// the rank-local halves of the 8-bit all-reduce (block maxima; codes with the shared scale;
+// sums of P ranks' codes and the dequantized output)
+int launch_q8_absmax(const void* x, bool in_bf16, int64_t n, float* amax, cudaStream_t stream, const char** why);
+int launch_q8_quantize(const void* x, bool in_bf16, int64_t n, const float* amax, int8_t* codes, float* scales,
+                       cudaStream_t stream, const char** why);
+int launch_q8_sum(int P, const int8_t* const* codes, const float* scales, int64_t n, void* out, bool out_bf16,
+                  int32_t* sums, cudaStream_t stream, const char** why);
 int launch_expire_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream, const char** why);
 int launch_out_proj(const OutProjArgs& a, const void* y, const void* W, int64_t ldy, int64_t ldw, bool out_bf16,
                     cudaStream_t stream, const char** why);

@@ -217,6 +217,124 @@ k_q8(const Q8Args a) {
     if (a.scales && sub == 0) a.scales[blk] = scale;
 }
 
+// ------------------------------------------------------------------ rank-local halves
+// A tensor-parallel rank cannot run k_q8 on the other ranks' partials: it sees only its own.
+// The same arithmetic then splits into (1) the rank's block maxima (k_q8_absmax; the
+// out_proj kernel emits them too), (2) after a MAX all-reduce of those maxima, the rank's
+// int8 codes with the shared per-block scale (k_q8_quantize), and (3) after the ranks'
+// codes are gathered, the int32 sums and the dequantized output (k_q8_sum).  Every step is
+// the same correctly rounded fp32 operation as in k_q8, so (3) o (2) o max(1) reproduces
+// k_q8's sums, scales and outputs bit for bit.
+
+// amax[j] = max |x_i| over block j (a NaN is ignored, an infinity kept).
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+k_q8_absmax(const void* x, int64_t n, float* amax) {
+    constexpr int NW = kVec * (int)sizeof(Tin) / 4;
+    const int64_t blk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
+    const int sub = (threadIdx.x & 31) % kLanesPerBlock;
+    const int64_t i0 = blk * kBlock + kVec * sub;
+    uint32_t w[NW];
+    load_words<Tin>(reinterpret_cast<const Tin*>(x), i0, n, w);      // zeros past n
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) m = fmaxf(m, fabsf(elem<Tin>(w, e)));
+#pragma unroll
+    for (int off = kLanesPerBlock / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (sub == 0 && blk * kBlock < n) amax[blk] = m;
+}
+
+// codes[i] = clamp(rne(x_i * inv_j), -127, 127), inv_j = 127 / amax[j] (0 when amax[j] is 0 or
+// not a number); scales[j] = amax[j] / 127 (0 likewise).
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+k_q8_quantize(const void* x, int64_t n, const float* amax_in, int8_t* codes, float* scales) {
+    constexpr int NW = kVec * (int)sizeof(Tin) / 4;
+    const int64_t blk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
+    const int sub = (threadIdx.x & 31) % kLanesPerBlock;
+    const int64_t i0 = blk * kBlock + kVec * sub;
+    if (i0 >= n) return;
+    const float amax = __ldg(amax_in + blk);
+    float inv = 0.f, scale = 0.f;
+    if (amax > 0.f) {
+        inv = __fdiv_rn(127.0f, amax);
+        scale = __fdiv_rn(amax, 127.0f);
+    }
+    uint32_t w[NW];
+    load_words<Tin>(reinterpret_cast<const Tin*>(x), i0, n, w);
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+        int qv = __float2int_rn(__fmul_rn(elem<Tin>(w, e), inv));   // a NaN converts to 0
+        qv = qv > 127 ? 127 : (qv < -127 ? -127 : qv);
+        packed[e >> 2] |= ((uint32_t)qv & 0xffu) << (8 * (e & 3));
+    }
+    if (i0 + kVec <= n) {
+        __stcs(reinterpret_cast<uint2*>(codes + i0), make_uint2(packed[0], packed[1]));
+    } else {
+        for (int e = 0; e < kVec; ++e)
+            if (i0 + e < n) codes[i0 + e] = (int8_t)((packed[e >> 2] >> (8 * (e & 3))) & 0xffu);
+    }
+    if (scales && sub == 0) scales[blk] = scale;
+}
+
+struct Q8SumArgs {
+    const int8_t* codes[kMaxPartials];
+    const float* scales;
+    int64_t n;
+    void* out;
+    int32_t* sums;
+};
+
+// S[i] = sum_p codes_p[i] (int32), out[i] = float(S[i]) * scale_j.
+template <typename Tout, int P>
+__global__ void __launch_bounds__(kThreads)
+k_q8_sum(const Q8SumArgs a) {
+    const int64_t blk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
+    const int sub = (threadIdx.x & 31) % kLanesPerBlock;
+    const int64_t i0 = blk * kBlock + kVec * sub;
+    if (i0 >= a.n) return;
+    int s[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) s[e] = 0;
+    const bool whole = i0 + kVec <= a.n;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        uint32_t w0 = 0u, w1 = 0u;
+        if (whole) {
+            const uint2 u = __ldcs(reinterpret_cast<const uint2*>(a.codes[p] + i0));
+            w0 = u.x;
+            w1 = u.y;
+        } else {
+            for (int e = 0; e < kVec; ++e)
+                if (i0 + e < a.n) {
+                    const uint32_t byte = (uint32_t)(uint8_t)a.codes[p][i0 + e];
+                    if (e < 4) w0 |= byte << (8 * e);
+                    else w1 |= byte << (8 * (e - 4));
+                }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            s[e] += (int)(w0 << (24 - 8 * e)) >> 24;                 // sign-extended byte e
+            s[4 + e] += (int)(w1 << (24 - 8 * e)) >> 24;
+        }
+    }
+    const float scale = __ldg(a.scales + blk);
+    float o[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) o[e] = __fmul_rn(__int2float_rn(s[e]), scale);   // float(S) is exact
+    store8(reinterpret_cast<Tout*>(a.out), i0, a.n, o);
+    if (a.sums) {
+        if (whole) {
+            __stcs(reinterpret_cast<int4*>(a.sums + i0), make_int4(s[0], s[1], s[2], s[3]));
+            __stcs(reinterpret_cast<int4*>(a.sums + i0) + 1, make_int4(s[4], s[5], s[6], s[7]));
+        } else {
+            for (int e = 0; e < kVec; ++e)
+                if (i0 + e < a.n) a.sums[i0 + e] = s[e];
+        }
+    }
+}
+
 }  // namespace
 
 int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream, const char** why) {
@@ -253,6 +371,70 @@ int launch_q8(const Q8Args& a, bool in_bf16, bool out_bf16, cudaStream_t stream,
         return -1;
     }
     return 0;
+}
+
+// One launch covers ceil(n / 128) blocks of 128 elements, 16 blocks per CTA.
+static bool q8_grid(int64_t n, dim3* grid, const char** why) {
+    const int64_t nblk = (n + kBlock - 1) / kBlock;
+    const int64_t ctas = (nblk + kThreads / kLanesPerBlock - 1) / (kThreads / kLanesPerBlock);
+    if (ctas > 0x7fffffff) {
+        *why = "n too large for one launch";
+        return false;
+    }
+    *grid = dim3((unsigned)ctas);
+    return true;
+}
+
+static int q8_launched(const char** why) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return -1;
+    }
+    return 0;
+}
+
+int launch_q8_absmax(const void* x, bool in_bf16, int64_t n, float* amax, cudaStream_t stream, const char** why) {
+    dim3 grid;
+    if (!q8_grid(n, &grid, why)) return -1;
+    if (in_bf16) k_q8_absmax<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(x, n, amax);
+    else k_q8_absmax<float><<<grid, kThreads, 0, stream>>>(x, n, amax);
+    return q8_launched(why);
+}
+
+int launch_q8_quantize(const void* x, bool in_bf16, int64_t n, const float* amax, int8_t* codes, float* scales,
+                       cudaStream_t stream, const char** why) {
+    dim3 grid;
+    if (!q8_grid(n, &grid, why)) return -1;
+    if (in_bf16) k_q8_quantize<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(x, n, amax, codes, scales);
+    else k_q8_quantize<float><<<grid, kThreads, 0, stream>>>(x, n, amax, codes, scales);
+    return q8_launched(why);
+}
+
+int launch_q8_sum(int P, const int8_t* const* codes, const float* scales, int64_t n, void* out, bool out_bf16,
+                  int32_t* sums, cudaStream_t stream, const char** why) {
+    dim3 grid;
+    if (!q8_grid(n, &grid, why)) return -1;
+    Q8SumArgs a{};
+    for (int p = 0; p < P; ++p) a.codes[p] = codes[p];
+    a.scales = scales;
+    a.n = n;
+    a.out = out;
+    a.sums = sums;
+    switch (P) {
+#define SSM_Q8S_CASE(PP)                                                                          \
+        case PP:                                                                                \
+            if (out_bf16) k_q8_sum<__nv_bfloat16, PP><<<grid, kThreads, 0, stream>>>(a);        \
+            else k_q8_sum<float, PP><<<grid, kThreads, 0, stream>>>(a);                         \
+            break;
+        SSM_Q8S_CASE(1) SSM_Q8S_CASE(2) SSM_Q8S_CASE(3) SSM_Q8S_CASE(4)
+        SSM_Q8S_CASE(5) SSM_Q8S_CASE(6) SSM_Q8S_CASE(7) SSM_Q8S_CASE(8)
+#undef SSM_Q8S_CASE
+        default:
+            *why = "P out of range";
+            return -1;
+    }
+    return q8_launched(why);
 }
 
 }  // namespace ssm

@@ -348,6 +348,64 @@ def pin_q8_bounds(lib, P=4, n=4096 + 77, block=128):
 
 
 
+def _split_reduce(parts, block, lib):
+    """The rank-local halves composed: max of the ranks' block maxima, codes, sum."""
+    amax = np.max(np.stack([orc.q8_block_absmax(p, block, lib=lib) for p in parts]), 0)
+    q = [orc.q8_quantize_shared(p, amax, block, lib=lib) for p in parts]
+    for r in q[1:]:
+        assert np.array_equal(r["scales"], q[0]["scales"]), "ranks disagree on the shared scale"
+    s = orc.q8_sum_dequant([r["codes"] for r in q], q[0]["scales"], block, lib=lib)
+    return s, q
+
+
+def pin_q8_split_hand_cases(lib):
+    """The hand-derived cases (golden file) through the rank-local halves."""
+    for case in read_q8_cases():
+        for dtype in (torch.float32, torch.bfloat16):
+            parts = [torch.from_numpy(p).to(dtype) for p in case["p"]]
+            s, q = _split_reduce(parts, case["block"], lib)
+            assert np.array_equal(s["sums"], case["sums"]), (case["name"], s["sums"])
+            assert np.array_equal(q[0]["scales"], case["scales"]), (case["name"], q[0]["scales"])
+            if "out" in case:
+                assert np.array_equal(s["out_f32"], case["out"]), (case["name"], s["out_f32"])
+
+
+def pin_q8_split_composes_to_reduce(lib):
+    """Block maxima combined by max, shared-scale codes and their sum equal the local
+    reduction bit for bit (sums, scales, fp32 and bf16 outputs), for ragged lengths."""
+    for P, n, dtype, seed in ((1, 300, torch.float32, 7), (3, 128 * 9 + 5, torch.bfloat16, 8),
+                              (4, 4096, torch.bfloat16, 9), (8, 1000, torch.float32, 10)):
+        parts = make_partials(P, (n,), dtype=dtype, seed=seed)
+        ref = orc.q8_reduce(parts, 128, lib=lib)
+        s, q = _split_reduce(parts, 128, lib)
+        assert np.array_equal(s["sums"], ref["sums"]), (P, n, "sums")
+        assert np.array_equal(q[0]["scales"], ref["scales"]), (P, n, "scales")
+        assert np.array_equal(s["out_f32"], ref["out_f32"]), (P, n, "out")
+        assert np.array_equal(s["out_bf16"], ref["out_bf16"]), (P, n, "bf16 out")
+
+
+def pin_q8_split_round_trip(lib, n=128 * 5 + 33):
+    """Independent checks of each half: the block maxima are numpy's; every code lies in
+    [-127, 127] and dequantizes within half a scale of its value; a block of zeros gives
+    zero codes and scale; one code buffer dequantizes to code * scale."""
+    x = make_partials(1, (n,), dtype=torch.float32, seed=11)[0]
+    x[128:256] = 0.0
+    xs = x.numpy().astype(np.float64)
+    amax = orc.q8_block_absmax(x, 128, lib=lib)
+    ref = np.array([np.abs(xs[j:j + 128]).max() for j in range(0, n, 128)], np.float32)
+    assert np.array_equal(amax, ref), "block maxima"
+    q = orc.q8_quantize_shared(x, amax, 128, lib=lib)
+    c = q["codes"].astype(np.int64)
+    sc = np.repeat(q["scales"].astype(np.float64), 128)[:n]
+    assert np.all(np.abs(c) <= 127)
+    assert np.all(np.abs(c * sc - xs) <= sc / 2 + 4 * 2.0 ** -24 * np.abs(xs)), "half-scale round trip"
+    assert q["scales"][1] == 0.0 and not np.any(c[128:256]), "zero block"
+    assert np.array_equal(q["scales"], (amax / np.float32(127.0)).astype(np.float32)), "scale"
+    s = orc.q8_sum_dequant([q["codes"]], q["scales"], 128, lib=lib)
+    assert np.array_equal(s["sums"], q["codes"].astype(np.int32))
+    assert np.array_equal(s["out_f32"], (q["codes"].astype(np.float32) * np.repeat(q["scales"], 128)[:n]))
+
+
 def pin_out_proj_vs_matmul(lib):
     """The partial equals an independent fp64 matrix product of the widened inputs; absdot is
     |y| |W|^T; the block maxima are those of the row-major partial, the last block short."""
@@ -534,6 +592,7 @@ MIXER_PINS = [pin_brute_force, pin_brute_force_bf16, pin_short_sequence, pin_pre
               pin_state_caching,
               pin_decode_matches_brute, pin_split_invariance]
 SCAN_PINS = [pin_scan_sequential, pin_scan_chunked]
-Q8_PINS = [pin_q8_hand_cases, pin_q8_bounds]
+Q8_PINS = [pin_q8_hand_cases, pin_q8_bounds, pin_q8_split_hand_cases, pin_q8_split_composes_to_reduce,
+           pin_q8_split_round_trip]
 OUT_PROJ_PINS = [pin_out_proj_vs_matmul, pin_out_proj_identity_and_rank_one]
 ALL_PINS = MIXER_PINS + SCAN_PINS + Q8_PINS + OUT_PROJ_PINS + SSD_PINS

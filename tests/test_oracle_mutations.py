@@ -44,6 +44,17 @@ MUTATIONS = {
     "q8_per_partial_amax": ("for (int p = 0; p < P; ++p)\n            for (int64_t i = j0; i < j1; ++i) {",
                             "for (int p = 0; p < 1; ++p)\n            for (int64_t i = j0; i < j1; ++i) {"),
     "q8_output_scale": ("float o = (float)s * scale;", "float o = (float)s * inv;"),
+    "q8s_absmax_signed": ("const float v = fabsf(widen_f32(x, in_dtype, i));\n            if (v > m) m = v;",
+                          "const float v = widen_f32(x, in_dtype, i);\n            if (v > m) m = v;"),
+    "q8s_inv_128": ("            inv = 127.0f / a;\n", "            inv = 128.0f / a;\n"),
+    "q8s_truncates": ("float r = rintf(widen_f32(x, in_dtype, i) * inv);",
+                      "float r = truncf(widen_f32(x, in_dtype, i) * inv);"),
+    "q8s_clamp_126": ("r = r > 127.0f ? 127.0f : (r < -127.0f ? -127.0f : r);",
+                      "r = r > 126.0f ? 126.0f : (r < -126.0f ? -126.0f : r);"),
+    "q8s_sum_skips_last_rank": ("for (int p = 0; p < P; ++p) s += codes[p][i];",
+                                "for (int p = 0; p + 1 < P; ++p) s += codes[p][i];"),
+    "q8s_scale_of_next_block": ("const float o = (float)s * scales[i / block];",
+                                "const float o = (float)s * scales[(i + 1) / block];"),
     "out_proj_W_transposed": ("const double wv = widen(W, in_dtype, n * K + k);",
                               "const double wv = widen(W, in_dtype, k * N + n);"),
     "out_proj_drops_last_k": ("for (int64_t k = 0; k < K; ++k) {\n                const double yv",
