@@ -7,6 +7,9 @@
   MAX of the per-block absolute maxima, local int8 quantization, all-reduce SUM
   of the int32 codes, dequantization -- equals the local q8 reduction of the same
   P partials bit for bit (this is what q8_reduce_partials computes on one GPU).
+* tp.q8_all_reduce, the exchange as the library runs it between GPUs (block maxima, MAX
+  all-reduce, shared-scale int8 codes, all-gather of the codes, local sum), with its
+  rank-local arithmetic injected from the oracle: equal to the local reduction on every rank.
 * The benchmark's cross-rank timing: the slowest rank's time and the whole-job rate.
 """
 import os
@@ -85,6 +88,54 @@ def _quantized_allreduce(rank, world):
     assert np.array_equal(out, ref["out_f32"])
 
 
+class _OracleOps:
+    """The rank-local arithmetic of tp.q8_all_reduce from the oracle (CPU), so the exchange's
+    control flow -- which collective, on which buffers, in which order -- runs on gloo ranks."""
+
+    @staticmethod
+    def block_absmax(x):
+        import oracle
+        return torch.from_numpy(oracle.q8_block_absmax(x))
+
+    @staticmethod
+    def quantize_shared(x, amax):
+        import oracle
+        r = oracle.q8_quantize_shared(x, amax.numpy())
+        return torch.from_numpy(r["codes"]).reshape(x.shape), torch.from_numpy(r["scales"])
+
+    @staticmethod
+    def sum_dequant(codes, scales, out_dtype):
+        import oracle
+        r = oracle.q8_sum_dequant([c.numpy() for c in codes], scales.numpy())
+        if out_dtype == torch.bfloat16:
+            out = torch.from_numpy(r["out_bf16"].view(np.int16)).view(torch.bfloat16)
+        else:
+            out = torch.from_numpy(r["out_f32"])
+        return out, torch.from_numpy(r["sums"])
+
+
+def _tp_q8_all_reduce(rank, world, out_dtype):
+    import oracle
+    from selective_state_space_prefill_gb300 import tp
+    from selective_state_space_prefill_gb300.inputs import make_partials
+    parts = make_partials(world, (3, 1, 1000), dtype=torch.bfloat16, seed=33)
+    out, sums, scales = tp.q8_all_reduce(parts[rank], out_dtype=out_dtype, ops=_OracleOps)
+    ref = oracle.q8_reduce([p.reshape(-1) for p in parts])
+    assert out.shape == parts[rank].shape and out.dtype == out_dtype
+    assert np.array_equal(sums.numpy(), ref["sums"])
+    assert np.array_equal(scales.numpy(), ref["scales"])
+    got = out.reshape(-1)
+    if out_dtype == torch.bfloat16:
+        assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), ref["out_bf16"])
+    else:
+        assert np.array_equal(got.numpy(), ref["out_f32"])
+    # every rank ends with the same result
+    mine = got.float().clone()
+    total = mine.clone()
+    dist.all_reduce(total)
+    assert torch.equal(total, mine * world)
+
+
 def _timing(rank, world):
     import bench
     t = bench.max_over_ranks(0.5 + rank)                  # rank r took 0.5 + r seconds
@@ -100,6 +151,13 @@ def test_channel_shards_gather_to_unsplit(world):
 @pytest.mark.parametrize("world", [2, 4])
 def test_quantized_allreduce_across_ranks_equals_local_q8(world):
     _run(world, _quantized_allreduce)
+
+
+@pytest.mark.parametrize("world,out_dtype", [(2, torch.float32), (4, torch.bfloat16)])
+def test_tp_q8_all_reduce_control_flow(world, out_dtype):
+    """tp.q8_all_reduce on gloo ranks: MAX all-reduce of block maxima, shared-scale codes,
+    all-gather of the int8 codes, local sum -- equal to the local reduction on every rank."""
+    _run(world, _tp_q8_all_reduce, out_dtype)
 
 
 def test_bench_cross_rank_timing():
