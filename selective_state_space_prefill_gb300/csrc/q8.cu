@@ -226,22 +226,31 @@ k_q8(const Q8Args a) {
 // the same correctly rounded fp32 operation as in k_q8, so (3) o (2) o max(1) reproduces
 // k_q8's sums, scales and outputs bit for bit.
 
+// Blocks per 16-lane group in the two single-partial kernels: one lane then has kGroupBlocks
+// independent 16-byte loads in flight, as the P-partial kernels have P.
+constexpr int kGroupBlocks = 4;
+
 // amax[j] = max |x_i| over block j (a NaN is ignored, an infinity kept).
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
 k_q8_absmax(const void* x, int64_t n, float* amax) {
     constexpr int NW = kVec * (int)sizeof(Tin) / 4;
-    const int64_t blk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
+    const int64_t grp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
     const int sub = (threadIdx.x & 31) % kLanesPerBlock;
-    const int64_t i0 = blk * kBlock + kVec * sub;
-    uint32_t w[NW];
-    load_words<Tin>(reinterpret_cast<const Tin*>(x), i0, n, w);      // zeros past n
-    float m = 0.f;
+    uint32_t w[kGroupBlocks][NW];
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) m = fmaxf(m, fabsf(elem<Tin>(w, e)));
+    for (int j = 0; j < kGroupBlocks; ++j)
+        load_words<Tin>(reinterpret_cast<const Tin*>(x), (grp * kGroupBlocks + j) * kBlock + kVec * sub, n, w[j]);
 #pragma unroll
-    for (int off = kLanesPerBlock / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (sub == 0 && blk * kBlock < n) amax[blk] = m;
+    for (int j = 0; j < kGroupBlocks; ++j) {
+        const int64_t blk = grp * kGroupBlocks + j;
+        float m = 0.f;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) m = fmaxf(m, fabsf(elem<Tin>(w[j], e)));
+#pragma unroll
+        for (int off = kLanesPerBlock / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (sub == 0 && blk * kBlock < n) amax[blk] = m;
+    }
 }
 
 // codes[i] = clamp(rne(x_i * inv_j), -127, 127), inv_j = 127 / amax[j] (0 when amax[j] is 0 or
@@ -250,32 +259,41 @@ template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
 k_q8_quantize(const void* x, int64_t n, const float* amax_in, int8_t* codes, float* scales) {
     constexpr int NW = kVec * (int)sizeof(Tin) / 4;
-    const int64_t blk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
+    const int64_t grp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kLanesPerBlock;
     const int sub = (threadIdx.x & 31) % kLanesPerBlock;
-    const int64_t i0 = blk * kBlock + kVec * sub;
-    if (i0 >= n) return;
-    const float amax = __ldg(amax_in + blk);
-    float inv = 0.f, scale = 0.f;
-    if (amax > 0.f) {
-        inv = __fdiv_rn(127.0f, amax);
-        scale = __fdiv_rn(amax, 127.0f);
-    }
-    uint32_t w[NW];
-    load_words<Tin>(reinterpret_cast<const Tin*>(x), i0, n, w);
-    uint32_t packed[2] = {0u, 0u};
+    uint32_t w[kGroupBlocks][NW];
+    float am[kGroupBlocks];
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-        int qv = __float2int_rn(__fmul_rn(elem<Tin>(w, e), inv));   // a NaN converts to 0
-        qv = qv > 127 ? 127 : (qv < -127 ? -127 : qv);
-        packed[e >> 2] |= ((uint32_t)qv & 0xffu) << (8 * (e & 3));
+    for (int j = 0; j < kGroupBlocks; ++j) {
+        const int64_t blk = grp * kGroupBlocks + j;
+        load_words<Tin>(reinterpret_cast<const Tin*>(x), blk * kBlock + kVec * sub, n, w[j]);
+        am[j] = blk * kBlock < n ? __ldg(amax_in + blk) : 0.f;
     }
-    if (i0 + kVec <= n) {
-        __stcs(reinterpret_cast<uint2*>(codes + i0), make_uint2(packed[0], packed[1]));
-    } else {
-        for (int e = 0; e < kVec; ++e)
-            if (i0 + e < n) codes[i0 + e] = (int8_t)((packed[e >> 2] >> (8 * (e & 3))) & 0xffu);
+#pragma unroll
+    for (int j = 0; j < kGroupBlocks; ++j) {
+        const int64_t blk = grp * kGroupBlocks + j;
+        const int64_t i0 = blk * kBlock + kVec * sub;
+        if (i0 >= n) break;
+        float inv = 0.f, scale = 0.f;
+        if (am[j] > 0.f) {
+            inv = __fdiv_rn(127.0f, am[j]);
+            scale = __fdiv_rn(am[j], 127.0f);
+        }
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            int qv = __float2int_rn(__fmul_rn(elem<Tin>(w[j], e), inv));   // a NaN converts to 0
+            qv = qv > 127 ? 127 : (qv < -127 ? -127 : qv);
+            packed[e >> 2] |= ((uint32_t)qv & 0xffu) << (8 * (e & 3));
+        }
+        if (i0 + kVec <= n) {
+            __stcs(reinterpret_cast<uint2*>(codes + i0), make_uint2(packed[0], packed[1]));
+        } else {
+            for (int e = 0; e < kVec; ++e)
+                if (i0 + e < n) codes[i0 + e] = (int8_t)((packed[e >> 2] >> (8 * (e & 3))) & 0xffu);
+        }
+        if (scales && sub == 0) scales[blk] = scale;
     }
-    if (scales && sub == 0) scales[blk] = scale;
 }
 
 struct Q8SumArgs {
@@ -396,7 +414,7 @@ static int q8_launched(const char** why) {
 
 int launch_q8_absmax(const void* x, bool in_bf16, int64_t n, float* amax, cudaStream_t stream, const char** why) {
     dim3 grid;
-    if (!q8_grid(n, &grid, why)) return -1;
+    if (!q8_grid((n + kGroupBlocks - 1) / kGroupBlocks, &grid, why)) return -1;
     if (in_bf16) k_q8_absmax<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(x, n, amax);
     else k_q8_absmax<float><<<grid, kThreads, 0, stream>>>(x, n, amax);
     return q8_launched(why);
@@ -405,7 +423,7 @@ int launch_q8_absmax(const void* x, bool in_bf16, int64_t n, float* amax, cudaSt
 int launch_q8_quantize(const void* x, bool in_bf16, int64_t n, const float* amax, int8_t* codes, float* scales,
                        cudaStream_t stream, const char** why) {
     dim3 grid;
-    if (!q8_grid(n, &grid, why)) return -1;
+    if (!q8_grid((n + kGroupBlocks - 1) / kGroupBlocks, &grid, why)) return -1;
     if (in_bf16) k_q8_quantize<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(x, n, amax, codes, scales);
     else k_q8_quantize<float><<<grid, kThreads, 0, stream>>>(x, n, amax, codes, scales);
     return q8_launched(why);
