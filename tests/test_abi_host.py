@@ -102,6 +102,48 @@ def test_q8_rejects_bad_arguments(lib, kw, code):
     assert _q8(lib, **kw) == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), INVALID), (dict(amax=None), INVALID), (dict(n=0), INVALID), (dict(block=256), UNSUPPORTED),
+    (dict(dtype=5), INVALID), (dict(x=FAKE + 2), MISALIGNED),
+])
+def test_q8_block_absmax_rejects_bad_arguments(lib, kw, code):
+    a = dict(x=FAKE, dtype=1, n=4096, block=128, amax=FAKE, stream=None)
+    a.update(kw)
+    assert lib.q8_block_absmax(*a.values()) == code
+    assert lib.ssm_last_error().decode().startswith("q8_block_absmax")
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), INVALID), (dict(amax=None), INVALID), (dict(codes=None), INVALID), (dict(n=0), INVALID),
+    (dict(block=64), UNSUPPORTED), (dict(dtype=3), INVALID), (dict(codes=FAKE + 8), MISALIGNED),
+    (dict(x=FAKE + 4), MISALIGNED), (dict(scales=FAKE + 2), MISALIGNED),
+])
+def test_q8_quantize_shared_rejects_bad_arguments(lib, kw, code):
+    a = dict(x=FAKE, dtype=1, n=4096, block=128, amax=FAKE, codes=FAKE, scales=None, stream=None)
+    a.update(kw)
+    assert lib.q8_quantize_shared(*a.values()) == code
+    assert lib.ssm_last_error().decode().startswith("q8_quantize_shared")
+
+
+def _q8_sum(lib, P=4, ptrs=None, **kw):
+    arr = (ctypes.c_void_p * max(P, 1))(*(ptrs or [FAKE] * max(P, 1)))
+    a = dict(P=P, codes=ctypes.cast(arr, ctypes.c_void_p), scales=FAKE, n=4096, block=128, out=FAKE,
+             out_dtype=1, sums=None, stream=None)
+    a.update(kw)
+    return lib.q8_sum_dequant(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(P=0), UNSUPPORTED), (dict(P=9), UNSUPPORTED), (dict(n=0), INVALID), (dict(block=32), UNSUPPORTED),
+    (dict(out=None), INVALID), (dict(scales=None), INVALID), (dict(codes=None), INVALID),
+    (dict(ptrs=[FAKE, None, FAKE, FAKE]), INVALID), (dict(ptrs=[FAKE, FAKE + 1, FAKE, FAKE]), MISALIGNED),
+    (dict(out_dtype=9), INVALID), (dict(sums=FAKE + 4), MISALIGNED),
+])
+def test_q8_sum_dequant_rejects_bad_arguments(lib, kw, code):
+    assert _q8_sum(lib, **kw) == code
+    assert lib.ssm_last_error().decode().startswith("q8_sum_dequant")
+
+
 def test_valid_call_without_gpu_fails_cleanly(lib):
     """A well-formed call on a machine without a usable GPU returns SSM_ERR_CUDA, not a crash."""
     import torch

@@ -126,6 +126,31 @@ def test_q8_and_out_proj_write_only_their_outputs():
         a.check("out_proj block maxima")
 
 
+def test_q8_halves_write_only_their_outputs():
+    n = 128 * 37 + 77                         # a short last block and a ragged last lane group
+    parts = [p.to(DEV) for p in make_partials(2, (n,), dtype=torch.bfloat16, seed=9)]
+    nblk = (n + 127) // 128
+    amax = Guarded((nblk,), torch.float32, float("nan"))
+    ssm.q8_block_absmax(parts[0], out=amax.view)
+    amax.check("q8_block_absmax")
+    shared = torch.maximum(amax.view, ssm.q8_block_absmax(parts[1]))
+    codes, scales = [], None
+    for p in parts:
+        c = Guarded((n,), torch.int8, 0x5A)
+        sc = Guarded((nblk,), torch.float32, float("nan"))
+        ssm.q8_quantize_shared(p, shared, codes=c.view, scales=sc.view)
+        _guards_intact(c, "q8_quantize_shared codes")
+        sc.check("q8_quantize_shared scales")
+        codes.append(c.view)
+        scales = sc.view
+    for out_dtype in (torch.bfloat16, torch.float32):
+        out = Guarded((n,), out_dtype, float("nan"))
+        sums = Guarded((n,), torch.int32, 0x5A5A5A5A)
+        ssm.q8_sum_dequant(codes, scales, out=out.view, sums=sums.view)
+        out.check(f"q8_sum_dequant {out_dtype} out")
+        sums.check("q8_sum_dequant sums")
+
+
 def _guards_intact(g, what):
     torch.cuda.synchronize()
     b = g.buf.cpu()
