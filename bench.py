@@ -680,7 +680,9 @@ def bench_ssd(ssm, dev, stream, hbm_peak, flush, tc_peak):
         del g
     res["note"] = ("k_ssd_pre (B, C conv + hi/lo planes, delta and decay sums) + k_ssd_chunk (tcgen05: G = C B^T, M X, C S^T and the "
                    "state update on bf16 hi/lo operand pairs, fp32 TMEM accumulators; a producer warp issues "
-                   "TMA and MMA, 16 worker warps the arithmetic).  frac_hbm is against algorithmic bytes; "
+                   "TMA and MMA, 16 worker warps the arithmetic; more rows than resident CTAs: one CTA per SM "
+                   "on an equal span of all rows' chunks, state handed on where a row is cut).  frac_hbm is "
+                   "against algorithmic bytes; "
                    "mma_TFLOP_s counts the hi/lo products the kernel issues (frac_tensor of the measured bf16 "
                    "peak); decode: k_ssd_decode + k_ssd_decode_shift per step, L2-resident state at batch 64")
     return res

@@ -376,7 +376,10 @@ int q8_sum_dequant(int P, const int8_t* const* codes, const float* scales, int64
  * returns SSM_ERR_UNSUPPORTED.
  */
 
-/* Bytes of device workspace ssd_prefill needs for these sizes (0 on a bad size). */
+/* Bytes of device workspace ssd_prefill needs for these sizes (0 on a bad size): the B and C
+ * channels after the conv as bf16 hi/lo operand planes, delta and the chunk-local decay sums,
+ * and min(batch * n_heads, 256) fp32 [64][64] state slots with their ready flags, through
+ * which a (row, head) pair cut between two CTAs of the chunk kernel passes its state. */
 size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_heads, int n_groups);
 
 /*
@@ -405,7 +408,11 @@ size_t ssd_prefill_workspace_bytes(int batch, int seqlen, int n_heads, int n_gro
  *   workspace, workspace_bytes     device memory of at least
  *                            ssd_prefill_workspace_bytes(batch, seqlen, n_heads, n_groups) bytes,
  *                            16-byte aligned, owned by the caller and not read afterwards
- * Asynchronous on cuda_stream (two kernels).  Returns SSM_OK or a negative status.
+ * Asynchronous on cuda_stream (two kernels).  When batch * n_heads exceeds the CTAs the GPU
+ * holds at once, the chunk kernel goes out as a cooperative launch of one CTA per resident
+ * slot, each walking an equal share of all rows' chunks; a launch the device refuses returns
+ * SSM_ERR_CUDA.  The result does not depend on how the rows were split.  Returns SSM_OK or a
+ * negative status.
  */
 int ssd_prefill(int batch, int seqlen, int n_heads, int head_dim, int n_groups, int d_state, int d_conv,
                 ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,

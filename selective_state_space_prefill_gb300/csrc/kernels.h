@@ -153,19 +153,26 @@ struct SsdArgs {
     int64_t out_stride_b, out_stride_t;
     float *conv_state_out, *ssm_state_out;
     void* workspace;                // B and C of every group after conv + SiLU, as bf16 hi/lo planes,
-                                    // then delta and the chunk-local decay sums per head
+                                    // then delta and the chunk-local decay sums per head, then the
+                                    // state hand-off slots and their flags
     int64_t ws_bt_off, ws_ds_off, ws_lp;   // filled in by launch_ssd_prefill
+    int64_t ws_ho_off, ws_flag_off;
+    int n_slots;
     unsigned int* status;
 };
 
 // Workspace of an SSD prefill: 4 planes [batch*G][L][64] (C hi, C lo, B hi, B lo), then at
 // bt_off 2 planes [batch*G][64][lp] (B hi, B lo, token-major), then at ds_off 2 fp32 planes
 // [batch*H][lp] (delta; s, the decay exponent summed from each 128-token chunk's start, in log2
-// units), lp = L rounded up to 128.
+// units), lp = L rounded up to 128; then at ho_off n_slots fp32 states [64][64] (a row cut
+// between two CTAs passes its state there) and at flag_off their n_slots uint32 ready flags.
 struct SsdWorkspace {
     size_t bytes;
-    int64_t bt_off, ds_off, lp;
+    int64_t bt_off, ds_off, lp, ho_off, flag_off;
+    int n_slots;
 };
+// Most CTAs an SSD prefill launch uses (and hand-off slots a workspace holds).
+constexpr int kSsdMaxCtas = 256;
 SsdWorkspace ssd_workspace_layout(int batch, int seqlen, int n_heads, int n_groups);
 
 // One-token SSD decode for a batch of requests, in place on the cached states of their slots.

@@ -28,12 +28,15 @@
 //                 planes [t][n] (the K-major operands of C B^T and C S^T) and, for B, also as
 //                 token-major planes [n][t] (the K-major operand of the state update); and, in
 //                 the same launch, delta and the chunk-local decay sums of every head.
-//   k_ssd_chunk   one CTA per (batch row, head) walks the row's chunks in order, so the fp32
-//                 state stays on chip: a producer warp brings the raw x (with a 3-token conv
-//                 halo), z, the B/C tiles and the chunk's delta and decay sums by TMA and issues
-//                 the MMAs; 16 worker warps compute the x conv and the operands they own (X, the
+//   k_ssd_chunk   a CTA walks chunks of (batch row, head) pairs in order, so the fp32 state
+//                 stays on chip: a producer warp brings the raw x (with a 3-token conv halo), z,
+//                 the B/C tiles and the chunk's delta and decay sums by TMA and issues the MMAs;
+//                 16 worker warps compute the x conv and the operands they own (X, the
 //                 state-update weights, M, S) into 128-byte-swizzled shared memory, read the
 //                 accumulators back with tcgen05.ld, and send the output tile out by TMA stores.
+//                 With no more rows than resident CTAs there is one CTA per row; with more, one
+//                 CTA per SM takes an equal span of all rows' chunks (no partly filled last
+//                 wave), and a row cut between two CTAs passes its state through the workspace.
 //   k_ssd_decode  one CTA per (request, head): the one-token recurrence on the cached state
 //                 [64 x 64] in place, then k_ssd_decode_shift moves the conv windows of the B
 //                 and C channels (shared by the heads of a group, so they move after every head
@@ -86,7 +89,10 @@ struct Smem {
     static constexpr int CB = CW + 1024;             // conv bias [64]
     static constexpr int BAR = CB + 256;             // nine mbarriers (TMA, MMA groups, hand-offs)
     static constexpr int SLOT = BAR + 80;            // TMEM base address, error flag
-    static constexpr int TOTAL = SLOT + 16;
+    static constexpr int SPAN = SLOT + 16;           // the CTA's span of chunks (SsdSpan, 64 bytes), the
+    static constexpr int ITEM = SPAN + 64;           // current item (b, h, c0, c1)
+    static constexpr int DH = ITEM + 16;             // and D of its head
+    static constexpr int TOTAL = DH + 16;
     static constexpr int ALLOC = TOTAL + 1024;       // + slack to align the base to 1024
     static constexpr int XR_BYTES = (kQ + 3) * kP * 2;
     static constexpr int TX_A = XR_BYTES + 4 * 8192 + 2 * 512;   // raw x + B^T hi/lo + delta, s
@@ -258,6 +264,10 @@ __device__ __forceinline__ void ssd_dt_block(const SsdArgs& p, int cx, int b, in
 __global__ void __launch_bounds__(256)
 k_ssd_pre(const SsdArgs p, int nbx, int n_bc, int ncx) {
     const int blk = blockIdx.x;
+    if (blk == 0) {                                  // the chunk kernel's hand-off flags start clear
+        unsigned int* flags = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(p.workspace) + p.ws_flag_off);
+        for (int e = threadIdx.x; e < p.n_slots; e += 256) flags[e] = 0u;
+    }
     if (blk < n_bc) {
         const int bx = blk % nbx, g = (blk / nbx) % p.n_groups, b = blk / (nbx * p.n_groups);
         ssd_bc_block<Tin_bf16>(p, bx, nbx, g, b);
@@ -293,6 +303,83 @@ __device__ __forceinline__ bool workers_any(bool v) {
     return r != 0;
 }
 
+// ------------------------------------------------------------------ work split
+// The chunks of all (batch row, head) pairs, flattened row-major (unit u = row * nch + c, row =
+// b H + h), are cut into gridDim.x contiguous spans of near-equal length, one per CTA.  A CTA
+// walks the pieces of rows ("items") its span covers; the state stays on chip within an item.
+// With more rows than CTAs every span holds at least nch units, so a row is cut at most once:
+// its head (chunks [0, c)) ends CTA i's span and its tail starts CTA i+1's.  CTA i walks that
+// head first and CTA i+1 the tail last, and the state at the cut passes through hand-off slot i
+// of the workspace behind a release/acquire flag; the tail's wait is then normally over before
+// it starts.  With no more rows than CTAs the launch has one CTA per row and nothing is cut.
+struct SsdItem {
+    int b, h, c0, c1;                                // chunks [c0, c1) of row (b, h)
+};
+
+struct SsdSpan {
+    int64_t u0, u1;                                  // units [u0, u1)
+    int nch, H, rf, rl;                              // chunks per row, heads, first and last row
+    bool head, tail;                                 // the span ends inside row rl / starts inside row rf
+
+    __device__ SsdSpan(int64_t rows, int nch_, int H_, int cta, int n_cta) : nch(nch_), H(H_) {
+        const int64_t total = rows * nch_;
+        const int64_t q = total / n_cta, r = total % n_cta;   // floor(i total / n) without overflow
+        u0 = q * cta + r * cta / n_cta;
+        u1 = q * (cta + 1) + r * (cta + 1) / n_cta;
+        if (u1 <= u0) {
+            rf = 0;
+            rl = -1;
+            head = tail = false;
+            return;
+        }
+        rf = (int)(u0 / nch_);
+        rl = (int)((u1 - 1) / nch_);
+        head = u1 < (int64_t)(rl + 1) * nch_;
+        tail = u0 > (int64_t)rf * nch_;
+    }
+    __device__ int n_items() const { return rl - rf + 1; }
+    // items in walking order: the head of a row the next CTA continues first, then whole rows,
+    // then the tail of a row the previous CTA began
+    __device__ SsdItem item(int j) const {
+        const int n = rl - rf + 1;
+        int r;
+        if (head && j == 0) r = rl;
+        else if (tail && j == n - 1) r = rf;
+        else r = rf + (tail ? 1 : 0) + (j - (head ? 1 : 0));
+        const int64_t base = (int64_t)r * nch;
+        SsdItem it;
+        it.b = r / H;
+        it.h = r % H;
+        it.c0 = (int)(u0 > base ? u0 - base : 0);
+        it.c1 = (int)(u1 - base < nch ? u1 - base : nch);
+        return it;
+    }
+};
+
+static_assert(sizeof(SsdSpan) <= Smem::ITEM - Smem::SPAN, "the span overlaps the item");
+static_assert(Smem::ITEM % 16 == 0 && Smem::SPAN % 8 == 0, "span and item alignment");
+
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Bounded wait for a hand-off flag to turn non-zero; returns the flag (0 if the wait ran out).
+__device__ __forceinline__ unsigned int flag_wait_bounded(const unsigned int* f, uint64_t limit_ns = 2000000000ull) {
+    unsigned int v = ld_acquire_gpu(f);
+    if (v) return v;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(256);
+        v = ld_acquire_gpu(f);
+        if (v) return v;
+        if (globaltimer_ns() - t0 > limit_ns) return 0u;
+    }
+}
+
 // hi/lo bf16 pairs of two floats, packed as (lo element in the low half)
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -323,15 +410,26 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const bool producer = warp == kWorkers / 32;
     const int q = warp & 3, cg = (warp >> 2) & (kWG - 1);
     const int i = 32 * q + lane;                     // a worker's token row of the chunk
-    const int h = blockIdx.x, b = blockIdx.y;
     const int H = p.n_heads, G = p.n_groups, L = p.seqlen;
-    const int g = h / (H / G), BG = p.batch * G, bg = b * G + g;
+    const int BG = p.batch * G, HG = H / G;
     const int64_t HP = (int64_t)H * kP, Cx = HP + 2 * (int64_t)G * kNs;
     const int nch = (L + kQ - 1) / kQ;
-    const float Dh = p.Dskip[h];
+    // the span lives in shared memory and each item's (b, h, c0, c1) beside it, so that the
+    // workers keep only the step and chunk counters in registers across the chunk loop
+    SsdSpan* s_span = reinterpret_cast<SsdSpan*>(sm + Smem::SPAN);
+    int* s_item = reinterpret_cast<int*>(sm + Smem::ITEM);        // b, h, c0, c1
+    float* s_Dh = reinterpret_cast<float*>(sm + Smem::DH);
+    // the hand-off slots [n_slots][64][64] and their flags [n_slots] in the workspace
+    auto slot_state = [&](int k) {
+        return reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + p.ws_ho_off) + (int64_t)k * kP * kNs;
+    };
+    auto slot_flag = [&](int k) {
+        return reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(p.workspace) + p.ws_flag_off) + k;
+    };
 
     if (tid == 0) {
         for (int k = 0; k < NBAR; ++k) mbar_init(&bars[k], k >= kXReady ? kWorkers / 32 : 1);
+        *s_span = SsdSpan((int64_t)p.batch * H, nch, H, (int)blockIdx.x, (int)gridDim.x);
         *s_err = 0;
         fence_barrier_init();
         prefetch_tmap(&tm_x);
@@ -340,27 +438,14 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         prefetch_tmap(&tm_bt);
     }
     if (warp == 0) tmem_alloc(slot, 512);
-    if (tid < kP) {
-        const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (h * (int64_t)kP + tid) * 4);
-        s_cw[4 * tid + 0] = w.x;
-        s_cw[4 * tid + 1] = w.y;
-        s_cw[4 * tid + 2] = w.z;
-        s_cw[4 * tid + 3] = w.w;
-        s_cb[tid] = p.conv_b[h * (int64_t)kP + tid];
-    }
+    __syncthreads();                                 // the span is in shared memory
+    const int n_items = s_span->n_items();
+    const int n_steps = (int)(s_span->u1 - s_span->u0);   // chunks this CTA walks
     // the state S[p][n] for p = i (workers with q < 2), n in [kCW cg, kCW cg + kCW): fp32 registers
     float S[kCW];
 #pragma unroll
     for (int k = 0; k < kCW; ++k) S[k] = 0.f;
-    if (!producer && q < 2 && p.ssm_state_in) {
-        const float4* src = reinterpret_cast<const float4*>(
-            p.ssm_state_in + (((int64_t)b * H + h) * kP + i) * kNs + kCW * cg);
-#pragma unroll
-        for (int k = 0; k < kCW / 4; ++k) {
-            const float4 v = src[k];
-            S[4 * k] = v.x; S[4 * k + 1] = v.y; S[4 * k + 2] = v.z; S[4 * k + 3] = v.w;
-        }
-    }
+    bool bad = false;                                // (workers) a wait of this worker ran out
     // S as the hi/lo operand tiles [p][n] that C S^T reads
     auto store_state = [&]() {
 #pragma unroll
@@ -373,7 +458,93 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             *reinterpret_cast<uint4*>(sm + Smem::SLO + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
         }
     };
-    if (!producer && q < 2) store_state();
+    // (workers) an item's per-head parameters and start state: the conv weights of the head's x
+    // channels, D, and S -- from ssm_state_in (or zeros) at a row's start, else from the hand-off
+    // slot of the CTA that walked the row's head.  Ends with a worker barrier.
+    auto begin_item = [&](int jt) {
+        const SsdItem it = s_span->item(jt);
+        if (tid == 0) {
+            s_item[0] = it.b;
+            s_item[1] = it.h;
+            s_item[2] = it.c0;
+            s_item[3] = it.c1;
+            *s_Dh = p.Dskip[it.h];
+        }
+        if (tid < kP) {
+            const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (it.h * (int64_t)kP + tid) * 4);
+            s_cw[4 * tid + 0] = w.x;
+            s_cw[4 * tid + 1] = w.y;
+            s_cw[4 * tid + 2] = w.z;
+            s_cw[4 * tid + 3] = w.w;
+            s_cb[tid] = p.conv_b[it.h * (int64_t)kP + tid];
+        }
+        const float* src = nullptr;
+        if (it.c0 == 0) {
+            if (p.ssm_state_in) src = p.ssm_state_in + ((int64_t)it.b * H + it.h) * kP * kNs;
+        } else {
+            unsigned int f = 1u;
+            if (tid == 0) {
+                f = flag_wait_bounded(slot_flag(blockIdx.x - 1));
+                if (f == 0u) atomicOr(p.status, 1u);
+            }
+            if (workers_any(f != 1u)) bad = true;
+            __threadfence();
+            src = slot_state(blockIdx.x - 1);
+        }
+        if (q < 2) {
+            if (src) {
+                const float4* s4 = reinterpret_cast<const float4*>(src + (int64_t)i * kNs + kCW * cg);
+#pragma unroll
+                for (int k = 0; k < kCW / 4; ++k) {
+                    const float4 v = __ldcg(s4 + k);
+                    S[4 * k] = v.x; S[4 * k + 1] = v.y; S[4 * k + 2] = v.z; S[4 * k + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kCW; ++k) S[k] = 0.f;
+            }
+            store_state();
+        }
+        fence_proxy_async_smem();
+        workers_sync();
+    };
+    // (workers) an item's end: at a row's end the final SSM state and the conv window of the head's
+    // x channels; else the state into this CTA's hand-off slot and its flag raised (2: an error).
+    auto end_item = [&]() {
+        const SsdItem it = {s_item[0], s_item[1], s_item[2], s_item[3]};
+        if (it.c1 == nch) {
+            if (bad) {
+                atomicOr(p.status, 1u);
+                return;
+            }
+            if (q < 2) {
+                float4* dst = reinterpret_cast<float4*>(p.ssm_state_out + (((int64_t)it.b * H + it.h) * kP + i) * kNs +
+                                                        kCW * cg);
+#pragma unroll
+                for (int k = 0; k < kCW / 4; ++k) dst[k] = make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]);
+            }
+            if (tid < 3 * kP) {
+                const int k = tid / kP, pp = tid % kP, t = L - 3 + k;
+                const int64_t ch = it.h * (int64_t)kP + pp;
+                float v = 0.f;
+                if (t >= 0)
+                    v = to_f32(reinterpret_cast<const Tin_bf16*>(p.xBC)[(int64_t)it.b * p.xbc_stride_b + (int64_t)t * p.xbc_stride_t + ch]);
+                else if (p.conv_state_in)
+                    v = p.conv_state_in[((int64_t)it.b * 3 + 3 + t) * Cx + ch];
+                p.conv_state_out[((int64_t)it.b * 3 + k) * Cx + ch] = v;
+            }
+        } else {
+            if (q < 2) {
+                float4* dst = reinterpret_cast<float4*>(slot_state(blockIdx.x) + (int64_t)i * kNs + kCW * cg);
+#pragma unroll
+                for (int k = 0; k < kCW / 4; ++k) __stcg(dst + k, make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]));
+            }
+            __threadfence();
+            const bool any_bad = workers_any(bad);
+            if (tid == 0) st_release_gpu(slot_flag(blockIdx.x), any_bad ? 2u : 1u);
+        }
+    };
+    if (!producer && n_items > 0) begin_item(0);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -385,25 +556,27 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
     if (producer) {
         if (lane == 0) {
-            auto issue_a = [&](int c) {              // raw x (with the 3-token halo) and B^T hi/lo
-                const int t0 = c * kQ;
+            // the copies of chunk c of item `it`, the kk-th chunk this CTA walks
+            auto issue_a = [&](const SsdItem& it, int c, int kk) {   // raw x (3-token halo), B^T hi/lo
+                const int t0 = c * kQ, bg = it.b * G + it.h / HG;
                 mbar_arrive_expect_tx(&bars[kBarA], Smem::TX_A);
-                tma_load_3d(sm + Smem::XR, &tm_x, &bars[kBarA], h * kP, t0 - 3, b);
+                tma_load_3d(sm + Smem::XR, &tm_x, &bars[kBarA], it.h * kP, t0 - 3, it.b);
                 // delta and s of the chunk into the parity buffers
-                tma_load_3d(sm + Smem::DL + (c & 1) * 512, &tm_ds, &bars[kBarA], t0, b * H + h, 0);
-                tma_load_3d(sm + Smem::CS + (c & 1) * 512, &tm_ds, &bars[kBarA], t0, (BG / G) * H + b * H + h, 0);
+                tma_load_3d(sm + Smem::DL + (kk & 1) * 512, &tm_ds, &bars[kBarA], t0, it.b * H + it.h, 0);
+                tma_load_3d(sm + Smem::CS + (kk & 1) * 512, &tm_ds, &bars[kBarA], t0, p.batch * H + it.b * H + it.h, 0);
                 for (int k = 0; k < 2; ++k)
                     for (int r = 0; r < 2; ++r)
                         tma_load_3d(sm + (k ? Smem::BTLO : Smem::BTHI) + r * 8192, &tm_bt, &bars[kBarA],
                                     t0 + 64 * r, 0, k * BG + bg);
             };
-            auto issue_b = [&](int c) {              // C hi, C lo, B hi, B lo
+            auto issue_b = [&](const SsdItem& it, int c) {           // C hi, C lo, B hi, B lo
+                const int bg = it.b * G + it.h / HG;
                 mbar_arrive_expect_tx(&bars[kBarB], 4 * 16384);
                 for (int k = 0; k < 4; ++k) tma_load_3d(sm + 16384 * k, &tm_bc, &bars[kBarB], 0, c * kQ, k * BG + bg);
             };
-            auto issue_z = [&](int c) {
+            auto issue_z = [&](const SsdItem& it, int c) {
                 mbar_arrive_expect_tx(&bars[kBarZ], kQ * kP * 2);
-                tma_load_3d(sm + Smem::ZT, &tm_z, &bars[kBarZ], h * kP, c * kQ, b);
+                tma_load_3d(sm + Smem::ZT, &tm_z, &bars[kBarZ], it.h * kP, c * kQ, it.b);
             };
             // phase parity of the c-th completion of a once-per-chunk barrier
             auto wait = [&](int k, int c) -> bool {
@@ -412,17 +585,22 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 atomicOr(p.status, 1u);
                 return false;
             };
-            int ia = 1, ib = 1, iz = 1;              // copies issued per group
+            int ia = 0, ib = 0, iz = 0;              // copies issued per group
             int ng = 0, nd = 0, ny = 0;              // MMA groups committed
-            issue_b(0);
-            issue_a(0);
-            issue_z(0);
-            int c = 0;
-            for (; c < nch; ++c) {
-                if (!wait(kBarB, c)) break;
-                if (c > 0) {
-                    if (!wait(kDone, c - 1)) break;  // every worker is past chunk c-1
-                    issue_z(c);
+            SsdItem it = n_items > 0 ? s_span->item(0) : SsdItem{0, 0, 0, 0};
+            int jt = 0, c = it.c0;                   // item and chunk of step ks
+            if (n_steps > 0) {
+                issue_b(it, c);
+                issue_a(it, c, 0);
+                issue_z(it, c);
+                ia = ib = iz = 1;
+            }
+            int ks = 0;
+            for (; ks < n_steps; ++ks) {
+                if (!wait(kBarB, ks)) break;
+                if (ks > 0) {
+                    if (!wait(kDone, ks - 1)) break; // every worker is past step ks-1
+                    issue_z(it, c);
                     ++iz;
                 }
                 tc_fence_after();
@@ -435,7 +613,7 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 mma_k64(tYe, sb + Smem::CLO, sb + Smem::SHI, kIdescN64, false);
                 mma_commit(&bars[kBarG]);
                 ++ng;
-                if (!wait(kXReady, c)) break;
+                if (!wait(kXReady, ks)) break;
                 tc_fence_after();
                 // dS^T = (w x)^T B: rows 0-63 from the hi part of w x, rows 64-127 from its lo part
                 // (the MN-major A operand's two 64-row blocks), each times B hi + B lo
@@ -452,7 +630,7 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 }
                 mma_commit(&bars[kBarD]);
                 ++nd;
-                if (!wait(kMReady, c)) break;
+                if (!wait(kMReady, ks)) break;
                 tc_fence_after();
                 // Y_intra = M X: A = M (K-major, two 64-column regions); B = X (MN-major [t][p]).
                 // M hi runs against X hi and X lo stacked along N (the X lo tile is the second
@@ -473,16 +651,27 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 }
                 mma_commit(&bars[kBarY]);
                 ++ny;
-                if (c + 1 < nch) {
-                    if (!wait(kBarD, c)) break;      // raw x (conv done) and B^T (dS done) are free
-                    issue_a(c + 1);
+                // the next step's chunk: the next of this item, else the first of the next item
+                SsdItem nx = it;
+                int nc = c + 1, nj = jt;
+                if (nc == it.c1 && jt + 1 < n_items) {
+                    nj = jt + 1;
+                    nx = s_span->item(nj);
+                    nc = nx.c0;
+                }
+                if (ks + 1 < n_steps) {
+                    if (!wait(kBarD, ks)) break;     // raw x (conv done) and B^T (dS done) are free
+                    issue_a(nx, nc, ks + 1);
                     ++ia;
-                    if (!wait(kBarY, c)) break;      // M over C, B (and G, Y_inter) are consumed
-                    issue_b(c + 1);
+                    if (!wait(kBarY, ks)) break;     // M over C, B (and G, Y_inter) are consumed
+                    issue_b(nx, nc);
                     ++ib;
                 }
+                it = nx;
+                c = nc;
+                jt = nj;
             }
-            if (c < nch) {
+            if (ks < n_steps) {
                 // stopped early: let every copy and MMA group still in flight finish (its last
                 // completion) before shared memory and TMEM go away
                 const int last[6] = {ia, ib, iz, ng, nd, ny};
@@ -493,7 +682,6 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     } else {
         float* s_dl2 = reinterpret_cast<float*>(sm + Smem::DL);   // [2][128]: delta by chunk parity
         float* s_cs2 = reinterpret_cast<float*>(sm + Smem::CS);   // [2][128]: s by chunk parity
-        bool bad = false;
         auto wait = [&](int k, int c) {
             if (!bad && !mbar_wait_bounded(&bars[k], (uint32_t)(c & 1))) {
                 bad = true;
@@ -504,13 +692,16 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[k]);
         };
-        for (int c = 0; c < nch; ++c) {
+        int ks = 0;                                  // chunks walked so far
+        for (int jt = 0; jt < n_items; ++jt) {
+          const int c1 = s_item[3];
+          for (int c = s_item[2]; c < c1; ++c, ++ks) {
             const int t0 = c * kQ;
-            float* s_dl = s_dl2 + (c & 1) * kQ;
-            float* s_cs = s_cs2 + (c & 1) * kQ;
+            float* s_dl = s_dl2 + (ks & 1) * kQ;
+            float* s_cs = s_cs2 + (ks & 1) * kQ;
 
             // ---- 2. conv + SiLU of x (raw x, B^T, delta and s of the chunk landed together)
-            wait(kBarA, c);
+            wait(kBarA, ks);
             const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
             {
                 // x of token i, positions kCW cg .., written as X hi/lo and as the state-update
@@ -520,6 +711,7 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 for (int k = 0; k < 4; ++k) {
                     const int row = i + k;                    // tile row of token t0 + i - 3 + k
                     if (c == 0 && row < 3 && p.conv_state_in) {
+                        const int b = s_item[0], h = s_item[1];
 #pragma unroll
                         for (int e = 0; e < kCW; ++e)
                             r[k][e] = p.conv_state_in[((int64_t)b * 3 + row) * Cx + h * (int64_t)kP + kCW * cg + e];
@@ -575,9 +767,10 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
             // ---- 3. M = G 2^(s_i - s_j) delta_j (j < i), M[i][i] = G[i][i] delta_i + D, as hi/lo
             //      over the C and B tiles: columns [kMJ cg, kMJ cg + kMJ) of row i
-            wait(kBarG, c);
+            wait(kBarG, ks);
             tc_fence_after();
             {
+                const float Dh = *s_Dh;
                 const int j0 = kMJ * cg;
                 if (j0 > 32 * q + 31) {                  // entirely above the diagonal
 #pragma unroll
@@ -624,7 +817,7 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             arrive(kMReady);
 
             // ---- 4. state: S = 2^(s_Q) S + dS (the accumulator's hi-part rows + lo-part rows)
-            wait(kBarD, c);
+            wait(kBarD, ks);
             tc_fence_after();
             {
                 float v[kCW];
@@ -654,8 +847,8 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             fence_proxy_async_smem();
 
             // ---- 5. out = (Y_intra + 2^(s_i) Y_inter) SiLU(z)   (Y_intra holds D x through M's diagonal)
-            wait(kBarY, c);
-            wait(kBarZ, c);
+            wait(kBarY, ks);
+            wait(kBarZ, ks);
             tc_fence_after();
             {
                 float yi[kCW], ye[kCW], y2[kCW];
@@ -707,35 +900,29 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             workers_sync();
             if (tid == 0 && !bad) {
                 constexpr int kBoxes = sizeof(Tout) == 4 ? 2 : 1;
+                const int b = s_item[0], h = s_item[1];
 #pragma unroll
                 for (int k = 0; k < kBoxes; ++k)
                     tma_store_3d(&tm_out, sm + Smem::XHI + k * 16384, h * kP + k * (kP / kBoxes), t0, b);
                 bulk_commit();
             }
-            tc_fence_before();
-            arrive(kDone);
+            if (c + 1 < c1) {
+                tc_fence_before();
+                arrive(kDone);
+            }
+          }
+          // the item ends: its state goes out (or on to the next CTA), and the next item's
+          // parameters and start state come in before its last chunk is reported done, so before
+          // the producer may issue the next item's products
+          end_item();
+          if (jt + 1 < n_items) {
+              workers_sync();                        // every worker is done with the ended item
+              begin_item(jt + 1);
+          }
+          tc_fence_before();
+          arrive(kDone);
         }
         if (tid == 0) bulk_wait_read();              // the last output tile has left shared memory
-        if (bad) {
-            if (tid == 0) atomicOr(p.status, 1u);
-        } else {
-            // final SSM state and the x channels' conv window
-            if (q < 2) {
-                float4* dst = reinterpret_cast<float4*>(p.ssm_state_out + (((int64_t)b * H + h) * kP + i) * kNs + kCW * cg);
-#pragma unroll
-                for (int k = 0; k < kCW / 4; ++k) dst[k] = make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]);
-            }
-            if (tid < 3 * kP) {
-                const int k = tid / kP, pp = tid % kP, t = L - 3 + k;
-                const int64_t ch = h * (int64_t)kP + pp;
-                float v = 0.f;
-                if (t >= 0)
-                    v = to_f32(reinterpret_cast<const Tin_bf16*>(p.xBC)[(int64_t)b * p.xbc_stride_b + (int64_t)t * p.xbc_stride_t + ch]);
-                else if (p.conv_state_in)
-                    v = p.conv_state_in[((int64_t)b * 3 + 3 + t) * Cx + ch];
-                p.conv_state_out[((int64_t)b * 3 + k) * Cx + ch] = v;
-            }
-        }
     }
     tc_fence_before();
     __syncthreads();
@@ -856,7 +1043,10 @@ SsdWorkspace ssd_workspace_layout(int batch, int seqlen, int n_heads, int n_grou
     w.lp = round_up(seqlen, kQ);
     w.bt_off = round_up(4 * BG * seqlen * kNs * 2, 256);
     w.ds_off = round_up(w.bt_off + 2 * BG * kNs * w.lp * 2, 256);
-    w.bytes = (size_t)(w.ds_off + 2 * BH * w.lp * 4);
+    w.n_slots = (int)(BH < kSsdMaxCtas ? BH : kSsdMaxCtas);
+    w.ho_off = round_up(w.ds_off + 2 * BH * w.lp * 4, 256);
+    w.flag_off = w.ho_off + (int64_t)w.n_slots * kP * kNs * 4;
+    w.bytes = (size_t)round_up(w.flag_off + (int64_t)w.n_slots * 4, 16);
     return w;
 }
 
@@ -866,6 +1056,9 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
     a.ws_bt_off = w.bt_off;
     a.ws_ds_off = w.ds_off;
     a.ws_lp = w.lp;
+    a.ws_ho_off = w.ho_off;
+    a.ws_flag_off = w.flag_off;
+    a.n_slots = w.n_slots;
     const int64_t HP = (int64_t)a.n_heads * kP, Cx = HP + 2 * (int64_t)a.n_groups * kNs;
     const int64_t BG = (int64_t)a.batch * a.n_groups;
     const int L = a.seqlen;
@@ -912,10 +1105,45 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
         return -1;
     }
     auto kern = out_bf16 ? k_ssd_chunk<__nv_bfloat16> : k_ssd_chunk<float>;
-    static ContextMemo attr[2];
+    static ContextMemo attr[2], occ[2];
     if (!opt_in_dynamic_smem(attr[out_bf16 ? 1 : 0], kern, Smem::ALLOC, why)) return -1;
-    kern<<<dim3((unsigned)a.n_heads, (unsigned)a.batch), kThAll, Smem::ALLOC, stream>>>(mx, mz, mbc, mbt, mo, mds, a);
-    e = cudaGetLastError();
+    // One CTA per (row, head) while they fit on the GPU at once; beyond that one CTA per resident
+    // slot, each on an equal span of the chunks, the rows cut between CTAs handing their state on.
+    // Those CTAs wait on one another, so they go out as a cooperative launch (all resident).
+    void* per_sm_v = nullptr;
+    if (!occ[out_bf16 ? 1 : 0].get(&per_sm_v, [&](void** out) {
+            int dev = 0, n_sm = 0, per_sm = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThAll, Smem::ALLOC) != cudaSuccess)
+                return false;
+            *out = reinterpret_cast<void*>((intptr_t)per_sm * n_sm);
+            return true;
+        })) {
+        *why = "occupancy query failed";
+        return -1;
+    }
+    const int64_t resident = (int64_t)reinterpret_cast<intptr_t>(per_sm_v);
+    const int64_t cap = resident < kSsdMaxCtas ? resident : kSsdMaxCtas;
+    if (cap < 1) {
+        *why = "k_ssd_chunk cannot be resident on this device";
+        return -1;
+    }
+    const int64_t rows = (int64_t)a.batch * a.n_heads;
+    const bool cut = rows > cap;
+    const unsigned n_cta = (unsigned)(cut ? cap : rows);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_cta);
+    cfg.blockDim = dim3(kThAll);
+    cfg.dynamicSmemBytes = Smem::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeCooperative;
+    la[0].val.cooperative = cut ? 1 : 0;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mx, mz, mbc, mbt, mo, mds, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return -1;

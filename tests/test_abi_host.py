@@ -280,14 +280,18 @@ def _ssd(lib, ws_bytes=1 << 30, **kw):
 
 def test_ssd_workspace_bytes(lib):
     # 4 bf16 planes [B*G][L][64], 2 bf16 planes [B*G][64][Lp], 2 fp32 planes [B*H][Lp]
-    # (Lp = L rounded up to 128; each part starts on a 256-byte boundary)
+    # (Lp = L rounded up to 128; each part starts on a 256-byte boundary), then min(B*H, 256)
+    # fp32 hand-off states [64][64] and as many uint32 flags (the total rounded up to 16 bytes)
     up = lambda v: (v + 255) // 256 * 256
+    up16 = lambda v: (v + 15) // 16 * 16
     a = up(4 * 4 * 2048 * 64 * 2)
     b = up(a + 2 * 4 * 64 * 2048 * 2)
-    assert lib.ssd_prefill_workspace_bytes(4, 2048, 80, 1) == b + 2 * 4 * 80 * 2048 * 4
+    c = up(b + 2 * 4 * 80 * 2048 * 4)
+    assert lib.ssd_prefill_workspace_bytes(4, 2048, 80, 1) == up16(c + 256 * 64 * 64 * 4 + 256 * 4)
     a = up(4 * 2 * 300 * 128)
     b = up(a + 2 * 2 * 64 * 384 * 2)
-    assert lib.ssd_prefill_workspace_bytes(1, 300, 4, 2) == b + 2 * 4 * 384 * 4
+    c = up(b + 2 * 4 * 384 * 4)
+    assert lib.ssd_prefill_workspace_bytes(1, 300, 4, 2) == up16(c + 4 * 64 * 64 * 4 + 4 * 4)
     assert lib.ssd_prefill_workspace_bytes(0, 300, 4, 2) == 0
     assert lib.ssd_prefill_workspace_bytes(1, 300, 3, 2) == 0           # groups must divide heads
 

@@ -196,3 +196,37 @@ def test_ssd_short_prefills_chain():
     assert_rms_close(torch.cat([o1, o2, o3], 1), ref["out"], TOL, "short chain out")
     assert_rms_close(s3, ref["ssm_state"], TOL, "short chain state")
     assert np.array_equal(c3.cpu().double().numpy(), ref["conv_state"])
+
+
+def _batch_row(inp, b):
+    kw = inp._kw()
+    for k in inp._TOKENS:
+        kw[k] = kw[k][b:b + 1].contiguous()
+    return type(inp)(**kw)
+
+
+@pytest.mark.parametrize("batch,H,G,L", [(2, 80, 1, 300), (3, 64, 2, 1000), (5, 40, 4, 129), (4, 80, 1, 2048)])
+def test_ssd_rows_cut_between_ctas_bit_exact(batch, H, G, L):
+    """More (batch row, head) pairs than CTAs the GPU holds at once: the launch splits the chunks
+    of all rows evenly over one CTA per SM, and a row cut between two CTAs hands its state from
+    one to the other through the workspace.  The result is bit-identical to running each batch
+    row alone (one CTA per head, nothing cut), from input states; heads on both sides of the
+    cuts match the oracle."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert batch * H > n_sm and H <= n_sm, "the case must cut rows and its batch rows alone must not"
+    inp = make_ssd_inputs(batch, L, H, n_groups=G, seed=batch * 1000 + L)
+    cs, ss = make_ssd_states(batch, H, 64, 64, inp.channels, seed=batch + L)
+    out, cso, sso = _gpu(inp, cs, ss)
+    for b in range(batch):
+        o1, c1, s1 = _gpu(_batch_row(inp, b), cs[b:b + 1], ss[b:b + 1])
+        torch.cuda.synchronize()
+        assert torch.equal(o1, out[b:b + 1]), f"row {b}: out differs from the cut launch"
+        assert torch.equal(s1, sso[b:b + 1]), f"row {b}: ssm_state differs from the cut launch"
+        assert torch.equal(c1, cso[b:b + 1]), f"row {b}: conv_state differs from the cut launch"
+    assert ssm.device_status() == 0
+    if L <= 1000:
+        heads = [0, H // 2, H - 1]
+        ref = _oracle(inp, cs, ss, heads=heads)
+        cols = np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
+        assert_rms_close(out[..., cols], ref["out"][..., cols], TOL, "cut rows out")
+        assert_rms_close(sso[:, heads], ref["ssm_state"][:, heads], TOL, "cut rows state")
