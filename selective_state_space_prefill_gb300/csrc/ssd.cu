@@ -1019,8 +1019,11 @@ k_ssd_decode_shift(const SsdDecodeArgs a) {
 }
 
 // 3-D tensor map (bf16 unless f32): dims {d0, d1, d2} (d0 innermost), byte strides {s1, s2}, box {b0, b1, 1}.
+// promote256: L2 fetches in 256-byte units (for boxes whose rows are contiguous beyond 128 bytes);
+// else 128-byte units, for boxes that take one head's 128-byte slice of each token row, whose
+// neighbouring slice another CTA reads at another time.
 bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-               uint32_t b0, uint32_t b1, bool swizzle, bool f32 = false) {
+               uint32_t b0, uint32_t b1, bool swizzle, bool f32 = false, bool promote256 = true) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -1030,7 +1033,8 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
     return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
                dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
@@ -1087,9 +1091,9 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
     // raw x and z arrive 128-byte swizzled, so that a lane reading its own token row of 128 bytes
     // hits all 32 banks across a warp
     if (!make_map3(&mx, a.xBC, (uint64_t)Cx, (uint64_t)L, (uint64_t)a.batch, (uint64_t)a.xbc_stride_t * 2, xs_b, kP,
-                   kQ + 3, true) ||
+                   kQ + 3, true, false, false) ||
         !make_map3(&mz, a.z, (uint64_t)HP, (uint64_t)L, (uint64_t)a.batch, (uint64_t)a.z_stride_t * 2, zs_b, kP, kQ,
-                   true) ||
+                   true, false, false) ||
         !make_map3(&mbc, ws, kNs, (uint64_t)L, (uint64_t)(4 * BG), kNs * 2, (uint64_t)L * kNs * 2, kNs, kQ, true) ||
         !make_map3(&mbt, ws + w.bt_off, (uint64_t)L, kNs, (uint64_t)(2 * BG), (uint64_t)w.lp * 2,
                    (uint64_t)w.lp * kNs * 2, 64, kNs, true) ||
