@@ -13,7 +13,7 @@ This file is named so that pytest collects it last.
 import pytest
 import torch
 
-from _gpu import assert_parity
+from _gpu import assert_parity, cpu_channels, oracle_prefill, sample_channels
 from selective_state_space_prefill_gb300 import binding as ssm
 from selective_state_space_prefill_gb300.inputs import make_mixer_inputs, make_states
 
@@ -43,6 +43,31 @@ def test_noalloc_matches_workspace_entry_on_consecutive_calls():
         for g, r, what in zip(got, ref, ("out", "conv_state", "ssm_state")):
             assert_parity(g, r.cpu().double().numpy(), dtype, f"noalloc {what} (L={L})")
             assert torch.equal(g, r), f"noalloc {what} differs from the workspace entry (L={L})"
+    assert ssm.device_status() == 0
+
+
+def test_noalloc_against_the_oracle():
+    """The entry point checked directly against the fp64 oracle, not only through the workspace
+    entry: a batch-1 bf16 row in 4 segments (sampled channels, the 2e-3 RMS bar) and an fp32 pair
+    of rows from cached states in 5 segments with a ragged tail (every channel, the fp32 bar)."""
+    for batch, L, D, dtype, seg, states in [(1, 2048, 1536, torch.bfloat16, 512, False),
+                                            (2, 300, 64, torch.float32, 64, True)]:
+        inp = make_mixer_inputs(batch, L, D, dtype=dtype, seed=L + 7)
+        cs = ss = None
+        if states:
+            cs, ss = make_states(batch, D, seed=5)
+        g = inp.to(DEV)
+        out, cso, sso = _prefill(g, seg, None if cs is None else cs.to(DEV), None if ss is None else ss.to(DEV),
+                                 noalloc=True)
+        torch.cuda.synchronize()
+        ch = sample_channels(D, 40) if D > 64 else list(range(D))
+        ix = torch.as_tensor(ch, device=DEV, dtype=torch.long)
+        ref = oracle_prefill(cpu_channels(inp, ch), None if cs is None else cs[:, :, ch],
+                             None if ss is None else ss[:, ch])
+        assert_parity(out.index_select(2, ix), ref["out"], dtype, f"noalloc out vs oracle (L={L})")
+        assert_parity(sso.index_select(1, ix), ref["ssm_state"], dtype, f"noalloc ssm_state vs oracle (L={L})")
+        assert torch.equal(cso.index_select(2, ix).cpu().double(), torch.as_tensor(ref["conv_state"])), \
+            f"noalloc conv_state vs oracle (L={L})"
     assert ssm.device_status() == 0
 
 
