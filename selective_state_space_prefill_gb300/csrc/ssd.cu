@@ -138,15 +138,16 @@ __device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, uint
 }
 
 // ------------------------------------------------------------------ pre-pass: B and C
-// One block of 256 threads: 64 tokens (block bx of nbx) x 64 states of group g of row b.  The raw
-// B and C channels of the block's tokens and their 3-token halo are staged in shared memory with
-// 16-byte loads first; the conv then reads them from there.
+// One block of 256 threads: kBcT tokens (block bx of nbx) x 64 states of group g of row b.  The
+// raw B and C channels of the block's tokens and their 3-token halo are staged in shared memory
+// with 16-byte loads first; the conv then reads them from there.
+constexpr int kBcT = 32;
 template <typename Tin>
 __device__ __forceinline__ void ssd_bc_block(const SsdArgs& p, int bx, int nbx, int g, int b) {
-    __shared__ __align__(16) __nv_bfloat16 raw_s[64 + 3][2][kNs];   // token row x (C, B) x state
+    __shared__ __align__(16) __nv_bfloat16 raw_s[kBcT + 3][2][kNs];  // token row x (C, B) x state
     __shared__ float hist[3][2][kNs];                                 // conv_state_in rows (first block)
-    __shared__ __nv_bfloat16 tr[2][kNs][64 + 8];                      // B hi / lo of the block, state-major
-    const int t0 = bx * 64;
+    __shared__ __nv_bfloat16 tr[2][kNs][kBcT + 8];                    // B hi / lo of the block, state-major
+    const int t0 = bx * kBcT;
     const int G = p.n_groups, BG = p.batch * G, bg = b * G + g, L = p.seqlen;
     const int64_t HP = (int64_t)p.n_heads * kP, Cx = HP + 2 * (int64_t)G * kNs;
     const Tin* xb = reinterpret_cast<const Tin*>(p.xBC) + (int64_t)b * p.xbc_stride_b;
@@ -155,13 +156,22 @@ __device__ __forceinline__ void ssd_bc_block(const SsdArgs& p, int bx, int nbx, 
     auto chan = [&](int which, int n) -> int64_t {                    // 0: C, 1: B
         return HP + (which ? 0 : (int64_t)G * kNs) + (int64_t)g * kNs + n;
     };
-    // rows r = 0 .. 66 hold tokens t0 - 3 + r; 8 bf16 per 16-byte vector, 8 vectors per 64 states
-    for (int e = threadIdx.x; e < (64 + 3) * 2 * 8; e += 256) {
+    // rows r = 0 .. kBcT + 2 hold tokens t0 - 3 + r; 8 bf16 per 16-byte vector, 8 vectors per 64
+    // states.  Every load of a thread is issued before the first store, so their latencies overlap.
+    constexpr int kVec = (kBcT + 3) * 2 * 8, kPer = (kVec + 255) / 256;
+    uint4 val[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = threadIdx.x + 256 * j;
         const int r = e / 16, which = (e / 8) & 1, v = e & 7, t = t0 - 3 + r;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (t >= 0 && t < L)
-            val = *reinterpret_cast<const uint4*>(xb + (int64_t)t * p.xbc_stride_t + chan(which, 8 * v));
-        *reinterpret_cast<uint4*>(&raw_s[r][which][8 * v]) = val;
+        val[j] = make_uint4(0, 0, 0, 0);
+        if (e < kVec && t >= 0 && t < L)
+            val[j] = *reinterpret_cast<const uint4*>(xb + (int64_t)t * p.xbc_stride_t + chan(which, 8 * v));
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = threadIdx.x + 256 * j;
+        if (e < kVec) *reinterpret_cast<uint4*>(&raw_s[e / 16][(e / 8) & 1][8 * (e & 7)]) = val[j];
     }
     if (t0 == 0 && threadIdx.x < 2 * kNs) {
         const int which = threadIdx.x / kNs, n = threadIdx.x % kNs;
@@ -173,31 +183,43 @@ __device__ __forceinline__ void ssd_bc_block(const SsdArgs& p, int bx, int nbx, 
     auto rawv = [&](int r, int which, int n) -> float {               // token t0 - 3 + r
         return (t0 == 0 && r < 3) ? hist[r][which][n] : __bfloat162float(raw_s[r][which][n]);
     };
-    for (int e = threadIdx.x; e < 64 * kNs; e += 256) {
-        const int tl = e / kNs, n = e % kNs, t = t0 + tl;
-        if (t >= L) continue;
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {          // 0: C (planes 0, 1), 1: B (planes 2, 3)
-            const int64_t c = chan(which, n);
-            const float4 w = *reinterpret_cast<const float4*>(p.conv_w + c * 4);
-            float xc = fmaf(w.x, rawv(tl, which, n), p.conv_b[c]);
-            xc = fmaf(w.y, rawv(tl + 1, which, n), xc);
-            xc = fmaf(w.z, rawv(tl + 2, which, n), xc);
-            xc = fmaf(w.w, rawv(tl + 3, which, n), xc);
+    {
+        // thread: channel n of C (which 0) or B (which 1), the half of the block's tokens `half`;
+        // the conv window moves along in registers and the plane pointers by one row
+        constexpr int kHalf = kBcT / 2;
+        const int n = threadIdx.x & 63, which = (threadIdx.x >> 6) & 1, half = threadIdx.x >> 7;
+        const int64_t c = chan(which, n);
+        const float4 w = *reinterpret_cast<const float4*>(p.conv_w + c * 4);
+        const float cb = p.conv_b[c];
+        const int kind = which ? 2 : 0;
+        const int tl0 = kHalf * half;
+        __nv_bfloat16* hi_p = bc + (((int64_t)kind * BG + bg) * L + t0 + tl0) * kNs + n;
+        __nv_bfloat16* lo_p = bc + (((int64_t)(kind + 1) * BG + bg) * L + t0 + tl0) * kNs + n;
+        float x0 = rawv(tl0, which, n), x1 = rawv(tl0 + 1, which, n), x2 = rawv(tl0 + 2, which, n);
+        const int n_tok = min(kHalf, L - t0 - tl0);
+#pragma unroll 4
+        for (int k = 0; k < n_tok; ++k) {
+            const float x3 = rawv(tl0 + k + 3, which, n);
+            float xc = fmaf(w.x, x0, cb);
+            xc = fmaf(w.y, x1, xc);
+            xc = fmaf(w.z, x2, xc);
+            xc = fmaf(w.w, x3, xc);
             __nv_bfloat16 hi, lo;
             split_bf16(silu_in<Tin>(xc), hi, lo);
-            const int kind = which ? 2 : 0;
-            bc[(((int64_t)kind * BG + bg) * L + t) * kNs + n] = hi;
-            bc[(((int64_t)(kind + 1) * BG + bg) * L + t) * kNs + n] = lo;
+            hi_p[(int64_t)k * kNs] = hi;
+            lo_p[(int64_t)k * kNs] = lo;
             if (which) {
-                tr[0][n][tl] = hi;
-                tr[1][n][tl] = lo;
+                tr[0][n][tl0 + k] = hi;
+                tr[1][n][tl0 + k] = lo;
             }
+            x0 = x1;
+            x1 = x2;
+            x2 = x3;
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < 2 * kNs * 64; e += 256) {
-        const int k = e / (kNs * 64), n = (e / 64) % kNs, tl = e % 64, t = t0 + tl;
+    for (int e = threadIdx.x; e < 2 * kNs * kBcT; e += 256) {
+        const int k = e / (kNs * kBcT), n = (e / kBcT) % kNs, tl = e % kBcT, t = t0 + tl;
         if (t < L) bt[(((int64_t)k * BG + bg) * kNs + n) * p.ws_lp + t] = tr[k][n][tl];
     }
     // the conv window of the B and C channels after the last token
@@ -215,52 +237,44 @@ __device__ __forceinline__ void ssd_bc_block(const SsdArgs& p, int bx, int nbx, 
 }
 
 // ------------------------------------------------------------------ pre-pass: delta and s
-// One block of 256 threads: chunk cx of row b, heads [64 hb, 64 hb + 64); four lanes per head, each
-// on 32 tokens of the 128-token chunk: delta = softplus(dt + dt_bias) (0 past L) and s, the running
-// sum of delta A log2(e) from the chunk's start (constant past L); the partial sums meet by shuffles.
-__device__ __forceinline__ void ssd_dt_block(const SsdArgs& p, int cx, int b, int hb) {
-    const int hq = threadIdx.x & 3, h = hb * 64 + (threadIdx.x >> 2);
-    const bool live = h < p.n_heads;
-    const int t0 = cx * kQ + 32 * hq, L = p.seqlen;
-    const int64_t BH = (int64_t)p.batch * p.n_heads;
-    const int hh = live ? h : 0;
-    const uint16_t* dtp = reinterpret_cast<const uint16_t*>(p.dt) + (int64_t)b * p.dt_stride_b + hh;
-    const float bias = p.dt_bias[hh], A2 = p.A[hh] * kLog2e;
-    uint16_t raw[32];
+// One warp per (batch row b, head h, 128-token chunk cx); lane l takes tokens [4 l, 4 l + 4) of
+// the chunk: delta = softplus(dt + dt_bias) (0 past L) and s, the running sum of delta A log2(e)
+// from the chunk's start (constant past L).  The lanes' partial sums meet in a warp scan, and
+// each plane's chunk row leaves as one contiguous 512-byte store of the warp.
+__device__ __forceinline__ void ssd_dt_warp(const SsdArgs& p, int cx, int b, int h) {
+    const int lane = threadIdx.x & 31, L = p.seqlen;
+    const int t0 = cx * kQ + 4 * lane;
+    const uint16_t* dtp = reinterpret_cast<const uint16_t*>(p.dt) + (int64_t)b * p.dt_stride_b + h;
+    const float bias = p.dt_bias[h], A2 = p.A[h] * kLog2e;
+    uint16_t raw[4];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        raw[k] = 0;
-        if (live && t0 + k < L) raw[k] = dtp[(int64_t)(t0 + k) * p.dt_stride_t];
-    }
-    float d[32], s[32], run = 0.f;
+    for (int k = 0; k < 4; ++k) raw[k] = t0 + k < L ? dtp[(int64_t)(t0 + k) * p.dt_stride_t] : (uint16_t)0;
+    float d[4], s[4], run = 0.f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < 4; ++k) {
         d[k] = t0 + k < L ? softplus_in<Tin_bf16>(__uint_as_float((uint32_t)raw[k] << 16) + bias) : 0.f;
         run = fmaf(d[k], A2, run);
         s[k] = run;
     }
-    // exclusive sum of the earlier quarters of the chunk
+    // exclusive sum of the earlier lanes' totals
     float inc = run;
 #pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, inc, o, 4);
-        if (hq >= o) inc += u;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
     }
     const float off = inc - run;
-    if (!live) return;
-    float4* dl = reinterpret_cast<float4*>(reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(p.workspace) +
-                                                                    p.ws_ds_off) + ((int64_t)b * p.n_heads + h) * p.ws_lp + t0);
-    float4* sc = dl + BH * p.ws_lp / 4;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        dl[k] = make_float4(d[4 * k], d[4 * k + 1], d[4 * k + 2], d[4 * k + 3]);
-        sc[k] = make_float4(s[4 * k] + off, s[4 * k + 1] + off, s[4 * k + 2] + off, s[4 * k + 3] + off);
-    }
+    float* dl = reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + p.ws_ds_off) +
+                ((int64_t)b * p.n_heads + h) * p.ws_lp + t0;
+    float* sc = dl + (int64_t)p.batch * p.n_heads * p.ws_lp;
+    *reinterpret_cast<float4*>(dl) = make_float4(d[0], d[1], d[2], d[3]);
+    *reinterpret_cast<float4*>(sc) = make_float4(s[0] + off, s[1] + off, s[2] + off, s[3] + off);
 }
 
 // Both pre-passes in one launch, so that they run side by side: blocks [0, n_bc) convolve B and C
-// (grid ceil(L / 64) x G x batch, flattened), the rest compute delta and s (lp / 128 x batch x
-// ceil(H / 64)).
+// (grid ceil(L / kBcT) x G x batch, flattened); the rest hold eight delta-and-s warps each, warp w
+// on head w % H of row (w / H) % batch, chunk w / (H batch): a block's warps are neighbouring
+// heads, whose dt values share each token's row.
 __global__ void __launch_bounds__(256)
 k_ssd_pre(const SsdArgs p, int nbx, int n_bc, int ncx) {
     const int blk = blockIdx.x;
@@ -272,8 +286,9 @@ k_ssd_pre(const SsdArgs p, int nbx, int n_bc, int ncx) {
         const int bx = blk % nbx, g = (blk / nbx) % p.n_groups, b = blk / (nbx * p.n_groups);
         ssd_bc_block<Tin_bf16>(p, bx, nbx, g, b);
     } else {
-        const int k = blk - n_bc;
-        ssd_dt_block(p, k % ncx, (k / ncx) % p.batch, k / (ncx * p.batch));
+        const int64_t w = (int64_t)(blk - n_bc) * 8 + (threadIdx.x >> 5);
+        const int64_t HB = (int64_t)p.n_heads * p.batch;
+        if (w < (int64_t)ncx * HB) ssd_dt_warp(p, (int)(w / HB), (int)((w / p.n_heads) % p.batch), (int)(w % p.n_heads));
     }
 }
 
@@ -1068,9 +1083,9 @@ int launch_ssd_prefill(const SsdArgs& a0, bool out_bf16, cudaStream_t stream, co
     const int L = a.seqlen;
 
     {
-        const int nbx = (L + 63) / 64, ncx = (int)(w.lp / kQ);
+        const int nbx = (L + kBcT - 1) / kBcT, ncx = (int)(w.lp / kQ);
         const int64_t n_bc = (int64_t)nbx * a.n_groups * a.batch;
-        const int64_t n_dt = (int64_t)ncx * a.batch * ((a.n_heads + 63) / 64);
+        const int64_t n_dt = ((int64_t)ncx * a.batch * a.n_heads + 7) / 8;
         if (n_bc + n_dt > 0x7fffffffLL) {
             *why = "too many pre-pass blocks";
             return -1;
