@@ -230,3 +230,34 @@ def test_ssd_rows_cut_between_ctas_bit_exact(batch, H, G, L):
         cols = np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
         assert_rms_close(out[..., cols], ref["out"][..., cols], TOL, "cut rows out")
         assert_rms_close(sso[:, heads], ref["ssm_state"][:, heads], TOL, "cut rows state")
+
+
+def test_ssd_cut_rows_inside_a_cuda_graph():
+    """The cut-rows launch (cooperative, one CTA per SM) captured in a CUDA graph and replayed:
+    every replay gives the bits of the direct call (the pre-pass clears the hand-off flags each
+    time, so a replay never sees the previous replay's flags)."""
+    batch, L, H, G = 2, 1000, 80, 1
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert batch * H > n_sm
+    inp = make_ssd_inputs(batch, L, H, n_groups=G, seed=91).to(DEV)
+    ws = torch.empty(ssm.ssd_prefill_workspace_bytes(batch, L, H, G), device=DEV, dtype=torch.uint8)
+    out = torch.empty(batch, L, 64 * H, device=DEV)
+    cso = torch.empty(batch, 3, inp.channels, device=DEV)
+    sso = torch.empty(batch, H, 64, 64, device=DEV)
+    args = (inp.xBC, inp.z, inp.dt, inp.conv_w, inp.conv_b, inp.A, inp.D, inp.dt_bias, H, G)
+    ref = [t.clone() for t in ssm.ssd_prefill(*args, workspace=ws)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ssm.ssd_prefill(*args, out=out, conv_state_out=cso, ssm_state_out=sso, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ssm.ssd_prefill(*args, out=out, conv_state_out=cso, ssm_state_out=sso, workspace=ws, stream=s)
+    for _ in range(3):
+        out.zero_()
+        sso.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref[0]) and torch.equal(cso, ref[1]) and torch.equal(sso, ref[2])
+    assert ssm.device_status() == 0
