@@ -205,8 +205,10 @@ def _batch_row(inp, b):
     return type(inp)(**kw)
 
 
-@pytest.mark.parametrize("batch,H,G,L", [(2, 80, 1, 300), (3, 64, 2, 1000), (5, 40, 4, 129), (4, 80, 1, 2048)])
-def test_ssd_rows_cut_between_ctas_bit_exact(batch, H, G, L):
+@pytest.mark.parametrize("batch,H,G,L,out_dtype", [(2, 80, 1, 300, torch.float32), (3, 64, 2, 1000, torch.float32),
+                                                    (5, 40, 4, 129, torch.float32), (4, 80, 1, 2048, torch.float32),
+                                                    (2, 96, 2, 777, torch.bfloat16)])
+def test_ssd_rows_cut_between_ctas_bit_exact(batch, H, G, L, out_dtype):
     """More (batch row, head) pairs than CTAs the GPU holds at once: the launch splits the chunks
     of all rows evenly over one CTA per SM, and a row cut between two CTAs hands its state from
     one to the other through the workspace.  The result is bit-identical to running each batch
@@ -216,9 +218,9 @@ def test_ssd_rows_cut_between_ctas_bit_exact(batch, H, G, L):
     assert batch * H > n_sm and H <= n_sm, "the case must cut rows and its batch rows alone must not"
     inp = make_ssd_inputs(batch, L, H, n_groups=G, seed=batch * 1000 + L)
     cs, ss = make_ssd_states(batch, H, 64, 64, inp.channels, seed=batch + L)
-    out, cso, sso = _gpu(inp, cs, ss)
+    out, cso, sso = _gpu(inp, cs, ss, out_dtype)
     for b in range(batch):
-        o1, c1, s1 = _gpu(_batch_row(inp, b), cs[b:b + 1], ss[b:b + 1])
+        o1, c1, s1 = _gpu(_batch_row(inp, b), cs[b:b + 1], ss[b:b + 1], out_dtype)
         torch.cuda.synchronize()
         assert torch.equal(o1, out[b:b + 1]), f"row {b}: out differs from the cut launch"
         assert torch.equal(s1, sso[b:b + 1]), f"row {b}: ssm_state differs from the cut launch"
@@ -228,7 +230,8 @@ def test_ssd_rows_cut_between_ctas_bit_exact(batch, H, G, L):
         heads = [0, H // 2, H - 1]
         ref = _oracle(inp, cs, ss, heads=heads)
         cols = np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
-        assert_rms_close(out[..., cols], ref["out"][..., cols], TOL, "cut rows out")
+        extra = half_ulp_bf16(ref["out"][..., cols]) if out_dtype == torch.bfloat16 else None
+        assert_rms_close(out[..., cols], ref["out"][..., cols], TOL, "cut rows out", extra=extra)
         assert_rms_close(sso[:, heads], ref["ssm_state"][:, heads], TOL, "cut rows state")
 
 
