@@ -264,3 +264,47 @@ def test_ssd_cut_rows_inside_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(out, ref[0]) and torch.equal(cso, ref[1]) and torch.equal(sso, ref[2])
     assert ssm.device_status() == 0
+
+
+def _head_range(inp, h0, h1):
+    """Heads [h0, h1) of a one-group layout with the shared B and C channels: a run of its own."""
+    hp, H = 64, inp.n_heads
+    sub = make_ssd_inputs(inp.xBC.shape[0], inp.xBC.shape[1], h1 - h0, n_groups=1, seed=0)
+    sub.xBC = torch.cat([inp.xBC[..., h0 * hp:h1 * hp], inp.xBC[..., H * hp:]], -1).contiguous()
+    sub.z = inp.z[..., h0 * hp:h1 * hp].contiguous()
+    sub.dt = inp.dt[..., h0:h1].contiguous()
+    sub.A, sub.D, sub.dt_bias = (t[h0:h1].contiguous() for t in (inp.A, inp.D, inp.dt_bias))
+    sub.conv_w = torch.cat([inp.conv_w[h0 * hp:h1 * hp], inp.conv_w[H * hp:]]).contiguous()
+    sub.conv_b = torch.cat([inp.conv_b[h0 * hp:h1 * hp], inp.conv_b[H * hp:]]).contiguous()
+    return sub
+
+
+def test_ssd_cuts_inside_one_batch_row_bit_exact():
+    """Batch 1 with 200 heads: more pairs than CTAs, so heads of the same row are cut between CTAs.
+    The output equals, bit for bit, two uncut runs of 100 heads each (heads never exchange data),
+    and sampled heads match the oracle."""
+    H, L = 200, 300
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert H > n_sm and H // 2 <= n_sm
+    inp = make_ssd_inputs(1, L, H, n_groups=1, seed=101)
+    out, cso, sso = _gpu(inp)
+    torch.cuda.synchronize()
+    for h0, h1 in ((0, H // 2), (H // 2, H)):
+        o, c, s = _gpu(_head_range(inp, h0, h1))
+        torch.cuda.synchronize()
+        assert torch.equal(o, out[..., 64 * h0:64 * h1]), f"heads {h0}-{h1}: out"
+        assert torch.equal(s, sso[:, h0:h1]), f"heads {h0}-{h1}: ssm_state"
+        assert torch.equal(c[..., :64 * (h1 - h0)], cso[..., 64 * h0:64 * h1]), f"heads {h0}-{h1}: conv_state"
+    heads = [0, 99, 100, 151, 152, 199]
+    ref = _oracle(inp, heads=heads)
+    cols = np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
+    assert_rms_close(out[..., cols], ref["out"][..., cols], TOL, "one-row cuts out")
+    assert_rms_close(sso[:, heads], ref["ssm_state"][:, heads], TOL, "one-row cuts state")
+    assert ssm.device_status() == 0
+
+
+def test_ssd_prefill_one_group_per_head():
+    """G = H: every head has its own B and C channels."""
+    inp = make_ssd_inputs(2, 300, 4, n_groups=4, seed=111)
+    e = _check(_gpu(inp), _oracle(inp), "G = H")
+    print(f"G = H: out {e[0]:.2e} state {e[1]:.2e}")
