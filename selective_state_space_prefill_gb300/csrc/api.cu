@@ -224,7 +224,7 @@ int prefill_impl(const char* fn, int batch, int seqlen, int d_inner, int d_state
 
 extern "C" {
 
-int ssm_abi_version(void) { return 107; }
+int ssm_abi_version(void) { return 108; }
 
 const char* ssm_last_error(void) { return g_err; }
 

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding.EXPORTS)
     for fn in names:
         assert hasattr(lib, fn), fn
-    assert lib.ssm_abi_version() == 107
+    assert lib.ssm_abi_version() == 108
 
 
 FAKE = 0x10000  # 64 KiB-aligned fake device address, never dereferenced
