@@ -309,6 +309,19 @@ def test_ssd_prefill_rejects_bad_arguments(lib, kw, code):
     assert lib.ssm_last_error().decode().startswith("ssd_prefill")
 
 
+def test_ssd_prefill_refuses_a_workspace_without_the_handoff_slots(lib):
+    # (batch 2, L 300, 4 heads, 1 group): the planes end at 528 384 bytes; the hand-off slots and
+    # their flags follow. A workspace sized for the planes alone, or one byte short, is refused
+    # on the host.
+    up = lambda v: (v + 255) // 256 * 256
+    planes = up(up(4 * 2 * 300 * 64 * 2) + 2 * 2 * 64 * 384 * 2) + 2 * 8 * 384 * 4
+    need = lib.ssd_prefill_workspace_bytes(2, 300, 4, 1)
+    assert planes == 528384 and need > planes
+    for ws_bytes in (planes, need - 1):
+        assert _ssd(lib, ws_bytes=ws_bytes) == INVALID
+        assert "workspace" in lib.ssm_last_error().decode()
+
+
 def _ssd_dec(lib, **kw):
     a = dict(batch=2, H=4, P=64, G=2, N=64, W=4, in_dtype=1, out_dtype=0, xBC=FAKE, z=FAKE, dt=FAKE,
              conv_w=FAKE, conv_b=FAKE, A=FAKE, D=FAKE, dt_bias=FAKE, cs=FAKE, ss=FAKE, n_slots=2, slot=None,
