@@ -308,3 +308,17 @@ def test_ssd_prefill_one_group_per_head():
     inp = make_ssd_inputs(2, 300, 4, n_groups=4, seed=111)
     e = _check(_gpu(inp), _oracle(inp), "G = H")
     print(f"G = H: out {e[0]:.2e} state {e[1]:.2e}")
+
+
+def test_ssd_prompt_full_size_sampled():
+    """The Zamba2-7B-like batch-1 prompt the bench times (16384 tokens, 112 heads of 64, one group):
+    every output and the final state of three heads against the oracle."""
+    inp = make_ssd_inputs(1, 16384, 112, n_groups=1, seed=0)
+    out, cso, sso = _gpu(inp)
+    torch.cuda.synchronize()
+    heads = [0, 57, 111]
+    ref = _oracle(inp, heads=heads)
+    cols = np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
+    e_out = assert_rms_close(out[..., cols], ref["out"][..., cols], TOL, "prompt out")
+    e_st = assert_rms_close(sso[:, heads], ref["ssm_state"][:, heads], TOL, "prompt state")
+    print(f"prompt 1 x 16384 x 112: out {e_out:.2e} state {e_st:.2e}")
