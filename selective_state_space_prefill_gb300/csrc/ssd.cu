@@ -92,7 +92,10 @@ struct Smem {
     static constexpr int SPAN = SLOT + 16;           // the CTA's span of chunks (SsdSpan, 64 bytes), the
     static constexpr int ITEM = SPAN + 64;           // current item (b, h, c0, c1)
     static constexpr int DH = ITEM + 16;             // and D of its head
-    static constexpr int TOTAL = DH + 16;
+    static constexpr int EC = DH + 16;               // column factors 2^(s_last - s_j) delta_j of the
+                                                     // three 32-column blocks that can lie wholly
+                                                     // below a warp's rows [96] f32
+    static constexpr int TOTAL = EC + 512;
     static constexpr int ALLOC = TOTAL + 1024;       // + slack to align the base to 1024
     static constexpr int XR_BYTES = (kQ + 3) * kP * 2;
     static constexpr int TX_A = XR_BYTES + 4 * 8192 + 2 * 512;   // raw x + B^T hi/lo + delta, s
@@ -718,6 +721,13 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             // ---- 2. conv + SiLU of x (raw x, B^T, delta and s of the chunk landed together)
             wait(kBarA, ks);
             const float s_i = s_cs[i], s_Q = s_cs[kQ - 1], dl_i = s_dl[i];
+            if (tid < 3 * 32) {
+                // for a block of M wholly below a warp's rows: 2^(s_i - s_j) = 2^(s_i - s_last)
+                // 2^(s_last - s_j), both exponents <= 0 (s falls along the chunk), s_last the
+                // block's last column; read after this step's worker barrier
+                float* s_ec = reinterpret_cast<float*>(sm + Smem::EC);
+                s_ec[tid] = ex2(s_cs[(tid & ~31) + 31] - s_cs[tid]) * s_dl[tid];
+            }
             {
                 // x of token i, positions kCW cg .., written as X hi/lo and as the state-update
                 // operand w_i x_i (w_i = 2^(s_Q - s_i) delta_i), hi and lo tiles
@@ -787,6 +797,7 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             {
                 const float Dh = *s_Dh;
                 const int j0 = kMJ * cg;
+                static_assert(kMJ == 32, "one 32-column block of M per thread");
                 if (j0 > 32 * q + 31) {                  // entirely above the diagonal
 #pragma unroll
                     for (int c8 = 0; c8 < kMJ / 8; ++c8) {
@@ -794,6 +805,27 @@ k_ssd_chunk(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         const uint32_t off = (uint32_t)((jj >> 6) * 16384 + i * 128 + ((((jj & 63) >> 3) ^ (i & 7)) << 4));
                         *reinterpret_cast<uint4*>(sm + Smem::MHI + off) = make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(sm + Smem::MLO + off) = make_uint4(0, 0, 0, 0);
+                    }
+                } else if (j0 + 31 < 32 * q) {           // entirely below: the factored decay
+                    const float* s_ec = reinterpret_cast<const float*>(sm + Smem::EC);
+                    const float er = ex2(s_i - s_cs[j0 + 31]);
+                    float v[32];
+                    tmem_ld32(tG + ((uint32_t)(32 * q) << 16) + (uint32_t)j0, v);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const float4 ea = *reinterpret_cast<const float4*>(s_ec + j0 + 8 * c8);
+                        const float4 eb = *reinterpret_cast<const float4*>(s_ec + j0 + 8 * c8 + 4);
+                        const float ej[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+                        float m[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) m[e] = v[8 * c8 + e] * (ej[e] * er);
+                        uint32_t whi[4], wlo[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) split2(m[2 * k], m[2 * k + 1], whi[k], wlo[k]);
+                        const int jj = j0 + 8 * c8;
+                        const uint32_t off = (uint32_t)((jj >> 6) * 16384 + i * 128 + ((((jj & 63) >> 3) ^ (i & 7)) << 4));
+                        *reinterpret_cast<uint4*>(sm + Smem::MHI + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+                        *reinterpret_cast<uint4*>(sm + Smem::MLO + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
                     }
                 } else {
 #pragma unroll
